@@ -1,0 +1,334 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each test is chosen so that a plausible slip in the oracle (a dropped RoPE
+term, a wrong sign, a transposed operand, an off-by-one in the causal range,
+a wrong page index, a wrong merge weight) fails at least one of them:
+
+* absorb == expand ("MLA inference: two computation paths and FlashMLA",
+  section "Two equivalent paths": the two paths give the same output; also
+  "FlashMLA: Fast Hopper Decoding for Latent Attention Guide", section
+  "Implementation: Simulating FlashMLA Decoding in Python", W_UK/W_UV shaped
+  [H, 128, 512]).  The expanded side is textbook multi-head attention in
+  numpy fp64, written here independently of the oracle.
+* split-merge == unsplit (the LSE merge of split-KV / chunked prefixes).
+* weights sum to one, brute force against a dense numpy formula, page
+  permutation invariance, and closed forms (uniform weights, one key,
+  a dominant key, duplicated keys).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import KV_BF16, KV_F64, KV_FP8, Problem
+
+
+def paged(keys_per_seq, page_size, rng, extra_pages=3):
+    """Scatter dense per-sequence key arrays [L_b, D] into a shuffled page pool."""
+    D = keys_per_seq[0].shape[1]
+    need = [(k.shape[0] + page_size - 1) // page_size for k in keys_per_seq]
+    pool_pages = sum(need) + extra_pages
+    perm = rng.permutation(pool_pages)
+    pool = rng.standard_normal((pool_pages, page_size, D))  # unused slots hold junk that must never be read
+    bt = np.full((len(keys_per_seq), max(need)), -1, np.int32)
+    o = 0
+    for b, k in enumerate(keys_per_seq):
+        for i in range(need[b]):
+            p = perm[o]
+            o += 1
+            bt[b, i] = p
+            rows = k[i * page_size:(i + 1) * page_size]
+            pool[p, :rows.shape[0]] = rows
+    return pool, bt
+
+
+def dense_reference(qn, qr, keys, scale, s_q, causal):
+    """softmax(scale * [qn|qr] K^T) C for one sequence; keys [L, d_c+d_r] dense fp64."""
+    d_c = qn.shape[-1]
+    L = keys.shape[0]
+    q = np.concatenate([qn, qr], axis=-1)            # [s_q, H, D]
+    s = scale * np.einsum("thd,jd->thj", q, keys)    # [s_q, H, L]
+    if causal:
+        for t in range(s_q):
+            s[t, :, max(0, L - s_q + 1 + t):] = -np.inf
+    m = s.max(axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    p = e / e.sum(axis=-1, keepdims=True)
+    out = np.einsum("thj,jd->thd", p, keys[:, :d_c])
+    lse = (m[..., 0] + np.log(e.sum(axis=-1)))
+    return out, lse
+
+
+# ---------------------------------------------------------------- absorb == expand
+
+def rope_rotate(x, pos):
+    """Rotate adjacent pairs of the last axis by angle pos / 10000^(2i/d) (decoupled RoPE)."""
+    d = x.shape[-1]
+    ang = pos[:, None] / 10000 ** (np.arange(0, d, 2) / d)
+    x1, x2 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x1 * np.cos(ang) - x2 * np.sin(ang)
+    out[..., 1::2] = x1 * np.sin(ang) + x2 * np.cos(ang)
+    return out
+
+
+@pytest.mark.parametrize("H,NOPE,ROPE,DV,DC,L,s_q,page", [
+    (4, 8, 4, 8, 16, 6, 6, 4),        # the page's toy shape: all 6 tokens are queries, causal
+    (128, 128, 64, 128, 512, 150, 2, 64),  # DeepSeek-V3 shape, two new tokens after 148 cached
+    (8, 128, 64, 128, 512, 70, 1, 64),     # single-token decode
+])
+def test_absorb_equals_expand(H, NOPE, ROPE, DV, DC, L, s_q, page):
+    rng = np.random.default_rng(1234 + H + L)
+    D = 64
+    h = rng.standard_normal((L, D))
+    W_q = rng.standard_normal((D, H * (NOPE + ROPE))) / 8
+    W_dkv = rng.standard_normal((D, DC)) / 8
+    W_kr = rng.standard_normal((D, ROPE)) / 8
+    W_uk = rng.standard_normal((H, DC, NOPE)) / 4   # latent -> per-head non-positional key
+    W_uv = rng.standard_normal((H, DC, DV)) / 4     # latent -> per-head value
+    pos = np.arange(L, dtype=np.float64)
+    c = h @ W_dkv                                   # [L, DC] cached latent
+    k_r = rope_rotate(h @ W_kr, pos)                # [L, ROPE] cached shared RoPE key
+    q = (h @ W_q).reshape(L, H, NOPE + ROPE)
+    q_n, q_r = q[..., :NOPE], rope_rotate(q[..., NOPE:].transpose(1, 0, 2), pos).transpose(1, 0, 2)
+    scale = 1 / math.sqrt(NOPE + ROPE)
+    new = np.arange(L - s_q, L)                     # positions of the new (query) tokens
+
+    # path one: expand K and V per head, ordinary causal multi-head attention
+    out1 = np.empty((s_q, H, DV))
+    for hh in range(H):
+        k = np.concatenate([c @ W_uk[hh], k_r], axis=1)     # [L, NOPE+ROPE]
+        v = c @ W_uv[hh]                                    # [L, DV]
+        qq = np.concatenate([q_n[new, hh], q_r[new, hh]], axis=1)
+        s = scale * qq @ k.T
+        s[np.arange(L)[None, :] > new[:, None]] = -np.inf
+        p = np.exp(s - s.max(1, keepdims=True))
+        p /= p.sum(1, keepdims=True)
+        out1[:, hh] = p @ v
+
+    # path two: absorb W_uk into the query, attend over the paged latent cache, apply W_uv last
+    q_lat = np.einsum("thn,hcn->thc", q_n[new], W_uk)       # [s_q, H, DC]
+    pool, bt = paged([np.concatenate([c, k_r], axis=1)], page, rng)
+    P = Problem(q_nope=q_lat[None], q_rope=q_r[new][None], kv=pool, kv_kind=KV_F64, block_table=bt,
+                seqlens=np.array([L], np.int32), scale=scale, causal=True, page_size=page)
+    out_lat, _ = P.full()
+    out2 = np.einsum("thc,hcv->thv", out_lat[0], W_uv)
+    np.testing.assert_allclose(out2, out1, rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- brute force vs dense formula
+
+@pytest.mark.parametrize("seed", range(6))
+def test_brute_force_tiny(seed):
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 4))
+    H = int(rng.integers(1, 5))
+    s_q = int(rng.integers(1, 3))
+    causal = bool(rng.integers(0, 2))
+    d_c, d_r, page = 32, 8, 16
+    Ls = rng.integers(s_q, 131, size=B)
+    keys = [rng.standard_normal((int(L), d_c + d_r)) for L in Ls]
+    pool, bt = paged(keys, page, rng)
+    qn = rng.standard_normal((B, s_q, H, d_c))
+    qr = rng.standard_normal((B, s_q, H, d_r))
+    scale = 1 / math.sqrt(192)
+    P = Problem(qn, qr, pool, KV_F64, bt, Ls.astype(np.int32), scale, causal=causal, page_size=page)
+    out, lse = P.full()
+    for b in range(B):
+        ro, rl = dense_reference(qn[b], qr[b], keys[b], scale, s_q, causal)
+        np.testing.assert_allclose(out[b], ro, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse[b], rl, rtol=1e-13, atol=1e-13)
+
+
+def test_visible_keys_causal_and_not():
+    rng = np.random.default_rng(5)
+    keys = [rng.standard_normal((10, 12))]
+    pool, bt = paged(keys, 4, rng)
+    qn, qr = rng.standard_normal((1, 3, 1, 8)), rng.standard_normal((1, 3, 1, 4))
+    Pc = Problem(qn, qr, pool, KV_F64, bt, np.array([10], np.int32), 0.3, causal=True, page_size=4)
+    Pn = Problem(qn, qr, pool, KV_F64, bt, np.array([10], np.int32), 0.3, causal=False, page_size=4)
+    assert [Pc.visible_keys(0, t) for t in range(3)] == [8, 9, 10]
+    assert [Pn.visible_keys(0, t) for t in range(3)] == [10, 10, 10]
+
+
+# ---------------------------------------------------------------- LSE merge
+
+@pytest.mark.parametrize("seed", range(5))
+def test_split_merge_equals_unsplit(seed):
+    rng = np.random.default_rng(100 + seed)
+    d_c, d_r, page, H = 64, 16, 8, 3
+    L = int(rng.integers(1, 300))
+    keys = [rng.standard_normal((L, d_c + d_r)) * 2]
+    pool, bt = paged(keys, page, rng)
+    qn, qr = rng.standard_normal((1, 1, H, d_c)), rng.standard_normal((1, 1, H, d_r))
+    P = Problem(qn, qr, pool, KV_F64, bt, np.array([L], np.int32), 0.2, page_size=page)
+    ref_out, ref_lse = P.rows(0, 0)
+    n_parts = int(rng.integers(1, 8))
+    cuts = np.sort(rng.integers(0, L + 1, size=n_parts - 1))
+    bounds = [0, *cuts.tolist(), L]                   # may contain empty ranges
+    for h in range(H):
+        outs, lses = [], []
+        for lo, hi in zip(bounds[:-1], bounds[1:]):
+            o, l = P.rows(0, 0, heads=[h], k_lo=lo, k_hi=hi)
+            outs.append(o[0])
+            lses.append(l[0])
+        mo, ml = oracle.merge(np.array(outs), np.array(lses))
+        np.testing.assert_allclose(mo, ref_out[h], rtol=1e-12, atol=1e-13)
+        assert abs(ml - ref_lse[h]) < 1e-12
+
+
+def test_merge_all_empty_parts():
+    out, lse = oracle.merge(np.zeros((3, 5)), np.full(3, -np.inf))
+    assert lse == -np.inf and np.all(out == 0)
+
+
+# ---------------------------------------------------------------- invariants and closed forms
+
+def _simple_problem(rng, L, H=2, d_c=32, d_r=8, page=8, keys=None, qn=None, qr=None, scale=0.25):
+    keys = [rng.standard_normal((L, d_c + d_r))] if keys is None else keys
+    pool, bt = paged(keys, page, rng)
+    qn = rng.standard_normal((1, 1, H, d_c)) if qn is None else qn
+    qr = rng.standard_normal((1, 1, H, d_r)) if qr is None else qr
+    return Problem(qn, qr, pool, KV_F64, bt, np.array([L], np.int32), scale, page_size=page), keys[0]
+
+
+def test_weights_sum_to_one():
+    rng = np.random.default_rng(7)
+    L, d_c, d_r = 97, 32, 8
+    keys = rng.standard_normal((L, d_c + d_r)) * 3
+    a = rng.standard_normal(d_c)
+    keys[:, :d_c] = a                                  # every value row equals a  =>  out == sum_j p_j * a == a
+    P, _ = _simple_problem(rng, L, keys=[keys])
+    out, _ = P.rows(0, 0)
+    np.testing.assert_allclose(out, np.broadcast_to(a, out.shape), rtol=1e-14, atol=1e-14)
+
+
+def test_zero_query_gives_uniform_weights():
+    rng = np.random.default_rng(8)
+    L = 130
+    P, keys = _simple_problem(rng, L, qn=np.zeros((1, 1, 2, 32)), qr=np.zeros((1, 1, 2, 8)))
+    out, lse = P.rows(0, 0)
+    np.testing.assert_allclose(out, np.broadcast_to(keys[:, :32].mean(0), out.shape), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(lse, math.log(L), rtol=1e-15)
+
+
+def test_single_key():
+    rng = np.random.default_rng(9)
+    P, keys = _simple_problem(rng, 1)
+    out, lse = P.rows(0, 0)
+    q = np.concatenate([P.q_nope[0, 0], P.q_rope[0, 0]], axis=1)
+    np.testing.assert_array_equal(out, np.broadcast_to(keys[0, :32], out.shape))
+    np.testing.assert_allclose(lse, 0.25 * q @ keys[0], rtol=1e-14)
+
+
+def test_dominant_key():
+    rng = np.random.default_rng(10)
+    L, j0 = 50, 17
+    qn = rng.standard_normal((1, 1, 1, 32))
+    keys = rng.standard_normal((L, 40))
+    keys[j0, :32] = 40 * qn[0, 0, 0] / np.linalg.norm(qn)  # score of key j0 exceeds the rest by > 50
+    P, _ = _simple_problem(rng, L, H=1, keys=[keys], qn=qn, qr=np.zeros((1, 1, 1, 8)))
+    out, _ = P.rows(0, 0)
+    np.testing.assert_allclose(out[0], keys[j0, :32], rtol=1e-12, atol=1e-12)
+
+
+def test_duplicated_keys_add_ln2():
+    rng = np.random.default_rng(11)
+    L = 40
+    keys = rng.standard_normal((L, 40))
+    P1, _ = _simple_problem(rng, L, keys=[keys])
+    P2, _ = _simple_problem(rng, 2 * L, keys=[np.concatenate([keys, keys])], qn=P1.q_nope, qr=P1.q_rope)
+    o1, l1 = P1.rows(0, 0)
+    o2, l2 = P2.rows(0, 0)
+    np.testing.assert_allclose(o2, o1, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(l2, l1 + math.log(2), rtol=1e-14)
+
+
+def test_empty_sequence():
+    rng = np.random.default_rng(12)
+    pool = rng.standard_normal((2, 8, 40))
+    P = Problem(np.ones((1, 1, 2, 32)), np.ones((1, 1, 2, 8)), pool, KV_F64, np.array([[0]], np.int32),
+                np.array([0], np.int32), 0.3, page_size=8)
+    out, lse = P.rows(0, 0)
+    assert np.all(out == 0) and np.all(lse == -np.inf)
+
+
+def test_page_permutation_invariance():
+    rng = np.random.default_rng(13)
+    B, H, d_c, d_r, page = 3, 2, 32, 8, 8
+    Ls = np.array([5, 64, 41], np.int32)
+    keys = [rng.standard_normal((int(L), d_c + d_r)) for L in Ls]
+    pool, bt = paged(keys, page, rng)
+    qn, qr = rng.standard_normal((B, 1, H, d_c)), rng.standard_normal((B, 1, H, d_r))
+    o1, l1 = Problem(qn, qr, pool, KV_F64, bt, Ls, 0.3, page_size=page).full()
+    perm = rng.permutation(pool.shape[0])            # new physical position of every page
+    pool2 = np.empty_like(pool)
+    pool2[perm] = pool
+    bt2 = np.where(bt >= 0, perm[np.maximum(bt, 0)], -1).astype(np.int32)
+    o2, l2 = Problem(qn, qr, pool2, KV_F64, bt2, Ls, 0.3, page_size=page).full()
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ---------------------------------------------------------------- cache formats (exact widening)
+
+def test_e4m3_all_codes_against_torch_and_definition():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_f64(int(c)) for c in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got)) and nan.sum() == 2          # only S.1111.111
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert oracle.e4m3_to_f64(0x7E) == 448.0 and oracle.e4m3_to_f64(0xFE) == -448.0   # largest finite magnitude
+    assert oracle.e4m3_to_f64(0x01) == 2.0 ** -9 and oracle.e4m3_to_f64(0x08) == 2.0 ** -6
+
+
+def _bf16_bits(x):
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_bf16_cache_matches_f64_cache():
+    rng = np.random.default_rng(14)
+    L, page = 77, 64
+    pool_bits = _bf16_bits(rng.standard_normal((3, page, 576)))
+    pool_f64 = torch.from_numpy(pool_bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    bt = np.array([[2, 0]], np.int32)
+    qn, qr = rng.standard_normal((1, 1, 4, 512)), rng.standard_normal((1, 1, 4, 64))
+    a = Problem(qn, qr, pool_bits, KV_BF16, bt, np.array([L], np.int32), 1 / math.sqrt(192)).full()
+    b = Problem(qn, qr, pool_f64, KV_F64, bt, np.array([L], np.int32), 1 / math.sqrt(192)).full()
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_fp8_cache_matches_f64_cache():
+    import mla_workloads as mw
+    rng = np.random.default_rng(15)
+    n = 2 * 64
+    x = rng.standard_normal((n, 576)).astype(np.float32)
+    rows = mw.quantize_fp8_rows(x[:, :512], mw.to_bf16_bits(x[:, 512:]))
+    # dequantise with torch (library decode of the codes, times the stored float32 scale)
+    codes = torch.from_numpy(rows[:, :512].copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    scales = rows[:, 512:528].copy().view(np.float32).astype(np.float64)
+    latent = codes * np.repeat(scales, 128, axis=1)
+    rope = torch.from_numpy(rows[:, 528:].copy().view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    pool_f64 = np.concatenate([latent, rope], axis=1).reshape(2, 64, 576)
+    # the quantiser really used its scale: each tile's largest magnitude maps to the top of the E4M3 range
+    assert np.allclose(np.abs(codes.reshape(n, 4, 128)).max(-1), 448.0)
+    bt = np.array([[1, 0]], np.int32)
+    qn, qr = rng.standard_normal((1, 2, 3, 512)), rng.standard_normal((1, 2, 3, 64))
+    L = np.array([100], np.int32)
+    a = Problem(qn, qr, rows.reshape(2, 64, 656), KV_FP8, bt, L, 1 / math.sqrt(192)).full()
+    b = Problem(qn, qr, pool_f64, KV_F64, bt, L, 1 / math.sqrt(192)).full()
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_threads_match_single_thread():
+    rng = np.random.default_rng(16)
+    Ls = np.array([33, 64, 130, 1], np.int32)
+    keys = [rng.standard_normal((int(L), 40)) for L in Ls]
+    pool, bt = paged(keys, 8, rng)
+    P = Problem(rng.standard_normal((4, 2, 3, 32)), rng.standard_normal((4, 2, 3, 8)), pool, KV_F64, bt, Ls, 0.3,
+                page_size=8)
+    a = P.full(threads=1)
+    b = P.full(threads=3)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
