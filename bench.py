@@ -1,0 +1,459 @@
+"""Benchmark of the absorbed-path MLA decode on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ragged] [--impl ours|reference]
+
+One step = one decode of the whole workload: the split-KV decode kernel plus
+the LSE combine (mla_decode_splitkv + mla_combine through the C ABI), inputs
+resident in HBM, L2 flushed before every step.  The scheduler metadata is
+computed once per step outside the timed region (it is reused by every layer
+of a decode step); the end-to-end leg (`e2e`) includes it together with the
+host<->device copies.
+
+Printed: one JSON line (rank 0).  `value` is the decode throughput as a
+percentage of one GB300's roofline, summed over GPUs: 100 * sum_r t_roof / T,
+t_roof = max(algorithmic bytes / HBM peak, algorithmic FLOPs / bf16 peak), T =
+the slowest rank's time per step.  Peaks come from MEASURED_PEAKS.json.
+
+With --impl reference the fp64 CPU oracle is timed on the host cores over a
+bounded sample of the same workload (the reference arm of this comparison).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode TFLOP/s and KV GB/s (B=64,H=128,ctx 4K–32K) as % of GB300 roofline"
+WORKLOAD_INDEX = {"tiny": 0, "uniform4k": 1, "ragged": 2, "long": 3, "fp8_mtp2": 4}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# ------------------------------------------------------------------ FLOP / byte accounting
+D_C, D_R = 512, 64
+
+
+def pair_flops(H: int, d_c: int = D_C, d_r: int = D_R) -> int:
+    """FLOPs of one (query token, key) pair on the absorbed path: QK over d_c+d_r dims and
+    PV over d_c dims for every head ("MLA inference: two computation paths and FlashMLA",
+    section "Which is faster: count new tokens and cached tokens", pair_absorb)."""
+    return 2 * H * (d_c + d_r) + 2 * H * d_c
+
+
+def causal_pairs(q: int, k: int) -> int:
+    """(query, key) pairs of q new tokens after k cached ones, k counting the new tokens, causal."""
+    return q * k - q * (q - 1) // 2
+
+
+def algorithmic_flops(seqlens, s_q: int, H: int, causal: bool = True) -> int:
+    pairs = sum(causal_pairs(s_q, int(L)) if causal else s_q * int(L) for L in seqlens)
+    return pairs * pair_flops(H)
+
+
+def algorithmic_bytes(seqlens, s_q: int, H: int, kv_row_bytes: int, out_elem_bytes: int) -> int:
+    """Bytes the decode must move at least once: every visible cache row (only the L_b
+    tokens, not the rest of the last page), the queries, outputs, LSE, used block-table
+    entries and the lengths."""
+    B = len(seqlens)
+    kv = sum(int(L) for L in seqlens) * kv_row_bytes
+    q = B * s_q * H * (D_C + D_R) * 2
+    out = B * s_q * H * D_C * out_elem_bytes
+    lse = B * s_q * H * 4
+    bt = sum((int(L) + 63) // 64 for L in seqlens) * 4
+    return kv + q + out + lse + bt + 4 * B
+
+
+def kv_bytes(seqlens, kv_row_bytes: int) -> int:
+    return sum(int(L) for L in seqlens) * kv_row_bytes
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def roofline_time_s(flops: int, nbytes: int, peaks) -> tuple[float, str]:
+    t_b = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_f = flops / (peaks["bf16_tflops"] * 1e12)
+    return (t_b, "hbm") if t_b >= t_f else (t_f, "tensor")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "mla_absorbed_decode_02_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM traffic per launch of the decode kernel from the committed ncu summary, if the
+    kernel sources still match the ones the counters were taken with."""
+    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks sampling
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(value: float, dist, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, dist, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
+def cpu_oracle_sample(w, budget_s: float, threads: int, rng_seed: int = 7):
+    """Time the fp64 oracle on whole (sequence, token) rows of w (all heads) until about
+    budget_s of wall time is spent; returns (seconds, pairs covered, rows done)."""
+    import oracle
+    P = oracle.from_workload(w)
+    rng = np.random.default_rng(rng_seed)
+    order = [(int(b), t) for b in rng.permutation(w.batch) for t in range(w.s_q)]
+    done, pairs = [], 0
+    t0 = time.perf_counter()
+    lock = threading.Lock()
+    idx = [0]
+
+    def worker():
+        nonlocal pairs
+        while True:
+            with lock:
+                if idx[0] >= len(order) or time.perf_counter() - t0 > budget_s:
+                    return
+                item = order[idx[0]]
+                idx[0] += 1
+            b, t = item
+            P.rows(b, t)
+            with lock:
+                done.append(item)
+                pairs += P.visible_keys(b, t)
+
+    ts = [threading.Thread(target=worker) for _ in range(threads)]
+    for th in ts:
+        th.start()
+    for th in ts:
+        th.join()
+    return time.perf_counter() - t0, pairs, len(done)
+
+
+def cpu_baseline(w, peaks, budget_s: float, threads: int):
+    secs, pairs, rows = cpu_oracle_sample(w, budget_s, threads)
+    H = w.num_heads
+    flops = pairs * pair_flops(H)
+    nbytes = pairs * (656 if w.kv_dtype == "fp8" else 1152)
+    t_roof, _ = roofline_time_s(flops, nbytes, peaks)
+    return {"value": 100.0 * t_roof / secs if secs > 0 else None, "unit": "% of GB300 roofline",
+            "cores": threads, "kind": "oracle", "tflops": flops / secs / 1e12,
+            "sample": f"{rows} of {w.batch * w.s_q} (sequence, token) rows, all {H} heads, "
+                      f"{pairs} (query, key) pairs, {secs:.1f} s wall on {threads} host threads"}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, w, peaks, world, rank, local):
+    import torch
+    from mla_absorbed_decode_02_gb300.build import build
+    from mla_absorbed_decode_02_gb300 import (Decoder, MlaDecodeParams, MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_OUT_BF16,
+                                              MLA_OUT_F32, mla_combine, mla_decode, mla_decode_splitkv,
+                                              mla_device_error, mla_get_scheduler_metadata)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        build()
+    dist = init_dist(world, "nccl")
+    if dist is not None:
+        dist.barrier()
+        build()
+
+    q_nope_h = torch.from_numpy(w.q_nope.view(np.int16)).view(torch.bfloat16)
+    q_rope_h = torch.from_numpy(w.q_rope.view(np.int16)).view(torch.bfloat16)
+    kv_h = torch.from_numpy(w.kv.view(np.int16)).view(torch.bfloat16) if w.kv_dtype == "bf16" else torch.from_numpy(w.kv)
+    bt_h = torch.from_numpy(w.block_table)
+    seq_h = torch.from_numpy(w.seqlens)
+    q_nope, q_rope, kv = q_nope_h.to(dev), q_rope_h.to(dev), kv_h.to(dev)
+    bt, seq = bt_h.to(dev), seq_h.to(dev)
+    p = MlaDecodeParams.make(w.batch, w.s_q, w.num_heads, w.num_pages, w.block_table.shape[1], causal=w.causal,
+                             kv_dtype=MLA_KV_FP8_E4M3 if w.kv_dtype == "fp8" else MLA_KV_BF16,
+                             out_dtype=MLA_OUT_F32 if w.out_dtype == "f32" else MLA_OUT_BF16)
+    dec = Decoder(p, dev)
+    out, lse = dec.new_outputs()
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # > L2 (129 MB)
+
+    mla_get_scheduler_metadata(p, seq, dec.sched, stream)
+
+    def step(ev=None):
+        if ev is None:
+            mla_decode_splitkv(p, q_nope, q_rope, kv, bt, seq, w.scale, out, lse, dec.sched, dec.workspace, stream)
+            mla_combine(p, out, lse, dec.sched, dec.workspace, stream)
+            return
+        ev[0].record(stream)
+        mla_decode_splitkv(p, q_nope, q_rope, kv, bt, seq, w.scale, out, lse, dec.sched, dec.workspace, stream)
+        ev[1].record(stream)
+        mla_combine(p, out, lse, dec.sched, dec.workspace, stream)
+        ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    assert mla_device_error(clear=True) == 0, "device error during warm-up"
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    for k in range(args.steps):
+        flush.zero_()
+        step(evs[k])
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    err = mla_device_error(clear=True)
+    assert err == 0, f"device error word {err}"
+    step_ms = [evs[k][0].elapsed_time(evs[k][2]) for k in range(args.steps)]
+    dec_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(args.steps)]
+    t_step = sum(step_ms) / len(step_ms) / 1e3
+    t_dec = sum(dec_ms) / len(dec_ms) / 1e3
+    t_max = reduce_max(t_step, dist, dev)
+
+    # ---- end to end through the public API: pinned host inputs -> device, plan, decode, results -> host
+    pin = lambda t: t.pin_memory()
+    hq, hr, hbt, hseq = pin(q_nope_h), pin(q_rope_h), pin(bt_h), pin(seq_h)
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hr, hbt, hseq))
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+
+    def e2e_step():
+        q_nope.copy_(hq, non_blocking=True)
+        q_rope.copy_(hr, non_blocking=True)
+        bt.copy_(hbt, non_blocking=True)
+        seq.copy_(hseq, non_blocking=True)
+        mla_get_scheduler_metadata(p, seq, dec.sched, stream)
+        mla_decode(p, q_nope, q_rope, kv, bt, seq, w.scale, out, lse, dec.sched, dec.workspace, stream)
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e_ms.append(a.elapsed_time(b))
+    t_e2e = reduce_max(sum(e_ms) / len(e_ms) / 1e3, dist, dev)
+    assert mla_device_error(clear=True) == 0
+
+    flops = algorithmic_flops(w.seqlens, w.s_q, w.num_heads, w.causal)
+    row_bytes = 656 if w.kv_dtype == "fp8" else 1152
+    nbytes = algorithmic_bytes(w.seqlens, w.s_q, w.num_heads, row_bytes, 4 if w.out_dtype == "f32" else 2)
+    t_roof, bound = roofline_time_s(flops, nbytes, peaks)
+    n = world
+    value = 100.0 * n * t_roof / t_max
+    if bound == "hbm":
+        achieved = nbytes / t_dec / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} (copy, burst)"}
+    else:
+        achieved = flops / t_dec / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "peak_source": f"{peaks['source']} (cuBLAS bf16, burst)"}
+    roof["traffic"] = committed_traffic(args.workload)
+    roof["kernel"] = "mla_decode_bf16_kernel"
+    roof["kernel_ms"] = t_dec * 1e3
+    res = {
+        "metric": METRIC, "value": value, "unit": "% of GB300 roofline (summed over GPUs)", "n_gpus": n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8-e4m3 cache, bf16 mma",
+        "data": "synthetic (seeded N(0,1) bf16 queries and cache, random page permutation)",
+        "config": {"workload": args.workload, "batch": w.batch, "heads": w.num_heads, "s_q": w.s_q,
+                   "seqlens": f"{int(w.seqlens.min())}..{int(w.seqlens.max())} (sum {int(w.seqlens.sum())})",
+                   "kv_dtype": w.kv_dtype, "pages": w.num_pages, "units": dec.num_units,
+                   "l2": "flushed before every step (256 MiB write)", "parallelism": f"replicas x{n}"},
+        "tflops": n * flops / t_max / 1e12, "kv_gbs": n * kv_bytes(w.seqlens, row_bytes) / t_max / 1e9,
+        "roofline": roof,
+        "e2e": {"value": 100.0 * n * t_roof / t_e2e, "unit": "% of GB300 roofline (summed over GPUs)",
+                "ms_per_step": t_e2e * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "includes": "H2D q/q_rope/block_table/seqlens, scheduler metadata, decode, D2H out/lse"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops", "source")},
+    }
+    return res, dist
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="ragged", choices=sorted(WORKLOAD_INDEX))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    import mla_workloads as mw
+
+    world, rank, local = dist_env()
+    peaks = load_peaks()
+    w = mw.make_workload(WORKLOAD_INDEX[args.workload])
+    threads = os.cpu_count() or 1
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        secs_total, pairs_total, rows_total = 0.0, 0, 0
+        per = max(2.0, min(args.cpu_budget, 60.0 / max(1, args.steps + args.warmup)))
+        for _ in range(args.warmup):
+            cpu_oracle_sample(w, per, threads)
+        for k in range(args.steps):
+            s, pr, rows = cpu_oracle_sample(w, per, threads, rng_seed=100 + k)
+            secs_total += s
+            pairs_total += pr
+            rows_total += rows
+        flops = pairs_total * pair_flops(w.num_heads)
+        nbytes = pairs_total * (656 if w.kv_dtype == "fp8" else 1152)
+        t_roof, _ = roofline_time_s(flops, nbytes, peaks)
+        value = 100.0 * t_roof / secs_total
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "% of GB300 roofline (summed over GPUs)",
+                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": secs_total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": args.workload, "batch": w.batch, "heads": w.num_heads,
+                           "sample": "each step: whole (sequence, token) rows for ~%.0f s" % per},
+                "cpu_baseline": {"value": value, "unit": "% of GB300 roofline", "cores": threads, "kind": "oracle",
+                                 "sample": f"{rows_total} rows, {pairs_total} (query, key) pairs, all heads, "
+                                           f"{secs_total:.1f} s over {args.steps} steps"},
+                "e2e": {"value": value, "unit": "% of GB300 roofline (summed over GPUs)", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    res, dist = run_ours(args, w, peaks, world, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(w, peaks, args.cpu_budget, threads)
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

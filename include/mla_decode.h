@@ -1,0 +1,183 @@
+/*
+ * mla_decode.h -- C ABI of libmla_decode.so: weight-absorbed Multi-Head Latent
+ * Attention decode on GB300 (sm_103a).
+ *
+ * The operation ("MLA inference: two computation paths and FlashMLA", section
+ * "Two equivalent paths", path two; "MLA: what the multi-head latent attention
+ * paper actually says", section "The absorbed form: how inference actually
+ * works"): every query head h of new token t of sequence b holds an absorbed
+ * query q~ (512 dims, W_UK already folded in by the caller) and a RoPE query
+ * q^R (64 dims).  Each cached token j holds a 512-dim latent c_j and a 64-dim
+ * RoPE key k^R_j shared by all heads (576 numbers per token).  The library
+ * computes
+ *     s_j = scale * (q~ . c_j + q^R . k^R_j)
+ *     out = sum_j softmax(s)_j * c_j        (512 dims, latent space; W_UV is NOT applied)
+ *     lse = ln sum_j exp(s_j)               (natural log, scale applied)
+ * over the keys the token may see.  The cache is paged, 64 tokens per page,
+ * addressed through a per-sequence block table ("FlashMLA: Fast Hopper
+ * Decoding for Latent Attention Guide", section "1. Direct Paged Latent
+ * Ingestion (512 + 64)"); long sequences are split across SMs and the partial
+ * results are merged through their LSE (split-KV, "MLA inference: two
+ * computation paths and FlashMLA", section "Decode attention becomes a compute
+ * problem"), with the split plan computed on the device from the context
+ * lengths (the "scheduling metadata precomputed from context lengths" of the
+ * same section).
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are CUDA device pointers on the current device;
+ *     "host" pointers are ordinary host memory.  All device buffers are owned
+ *     by the caller; the library never allocates or frees device memory and
+ *     never synchronises on the decode path.  Device buffers must be
+ *     contiguous in the stated layout and 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls are asynchronous on that stream.
+ *   - Return value: an mla_status.  Problems the host can see (null pointers,
+ *     bad sizes, unsupported options, a CUDA launch error) are returned at
+ *     once and nothing is launched.  Problems only the device can see (a
+ *     bounded wait that ran out) are recorded in a per-device error word that
+ *     mla_device_error() reads; outputs of such a call are undefined.
+ *   - Not thread-safe per (device, stream) for concurrent calls sharing one
+ *     workspace.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned buffer */
+  MLA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (e.g. H > 128, s_q > 2) */
+  MLA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed (no device, launch failure, ...) */
+  MLA_ERR_TIMEOUT = 4,      /* device error word: a bounded wait inside a kernel ran out */
+  MLA_ERR_WORKSPACE = 5,    /* scheduler metadata does not match the params (wrong unit count or batch) */
+} mla_status;
+
+typedef enum {
+  MLA_KV_BF16 = 0,          /* page = [64][576] bf16: c (512) then k^R (64); 1152 bytes per token */
+  MLA_KV_FP8_E4M3 = 1,      /* page = [64][656 bytes]: 512 E4M3 codes of c, then 4 float32 scales
+                               (one per 128-code tile, value = code * scale), then k^R as 64 bf16 */
+} mla_kv_dtype;
+
+typedef enum {
+  MLA_OUT_BF16 = 0,
+  MLA_OUT_F32 = 1,
+} mla_out_dtype;
+
+/* Problem description shared by all calls of one decode step. */
+typedef struct mla_decode_params {
+  int32_t batch;             /* B >= 1 sequences */
+  int32_t s_q;               /* new tokens per sequence: 1 or 2 */
+  int32_t num_heads;         /* H, 1..128 query heads */
+  int32_t num_pages;         /* physical pages in the pool (>= 1) */
+  int32_t page_size;         /* tokens per page; must be 64 */
+  int32_t max_pages_per_seq; /* row length of block_table (>= 1) */
+  int32_t causal;            /* s_q > 1: nonzero => new token t sees keys 0 .. L_b - s_q + t;
+                                zero => every new token sees all L_b keys */
+  int32_t kv_dtype;          /* mla_kv_dtype */
+  int32_t out_dtype;         /* mla_out_dtype */
+  int32_t num_units;         /* work units (one 2-SM cluster each); 0 = as many as fit at once */
+  int32_t timeout_us;        /* limit of every bounded wait inside the kernels; 0 = 2,000,000 us */
+  int32_t reserved[5];       /* must be zero */
+} mla_decode_params;
+
+/*
+ * Sizes of the two caller-provided device buffers for a decode with `p`:
+ *   *sched_bytes     -- scheduler metadata written by mla_get_scheduler_metadata
+ *   *workspace_bytes -- split partials (float32) used by mla_decode
+ * Both depend only on p (batch, s_q, num_heads, unit count), never on the
+ * context lengths, so buffers can be allocated once and reused.  Needs a CUDA
+ * device only when p->num_units == 0 (to count SMs).
+ */
+int32_t mla_get_workspace_size(const mla_decode_params* p, size_t* sched_bytes, size_t* workspace_bytes);
+
+/*
+ * Split plan ("which stretches of KV each SM handles"): reads the per-sequence
+ * lengths cache_seqlens (device, int32 [B], each length counts the s_q new
+ * tokens) and writes `sched` (device, sched_bytes).  One tiny kernel; no host
+ * synchronisation.  Compute it once per decode step and reuse it for every
+ * layer that shares the lengths.
+ */
+int32_t mla_get_scheduler_metadata(const mla_decode_params* p, const int32_t* cache_seqlens, void* sched,
+                                   void* stream);
+
+/*
+ * The decode.
+ *   q_nope_absorbed  device bf16 [B][s_q][H][512]  absorbed query q~
+ *   q_rope           device bf16 [B][s_q][H][64]   RoPE query q^R
+ *   kv_pages         device [num_pages][64][576] bf16, or [num_pages][64][656 bytes] FP8 rows
+ *   block_table      device int32 [B][max_pages_per_seq]: physical page of logical page i of
+ *                    sequence b; entries past ceil(L_b/64) are never read.  Every entry read
+ *                    must be in [0, num_pages).
+ *   cache_seqlens    device int32 [B]; L_b includes the s_q new tokens; 0 <= L_b <= 64*max_pages
+ *   scale            softmax scale (1/sqrt(192) for DeepSeek-V3 shapes)
+ *   out              device [B][s_q][H][512], bf16 or float32 (out_dtype)
+ *   lse              device float32 [B][s_q][H]; a token that sees no key gets out = 0, lse = -inf
+ *   sched            device, from mla_get_scheduler_metadata with the same p and lengths
+ *   workspace        device, workspace_bytes from mla_get_workspace_size
+ * Cache rows of the last page past L_b are not used (they may hold any bits).
+ */
+int32_t mla_decode(const mla_decode_params* p, const void* q_nope_absorbed, const void* q_rope, const void* kv_pages,
+                   const int32_t* block_table, const int32_t* cache_seqlens, float scale, void* out, float* lse,
+                   const void* sched, void* workspace, void* stream);
+
+/*
+ * The two halves of mla_decode, for callers that want to place or time them
+ * separately (same arguments and rules as mla_decode):
+ *   mla_decode_splitkv -- the decode kernel only: writes out/lse of every query
+ *                         token whose keys one unit handled, and the split
+ *                         partials (in workspace) of the others;
+ *   mla_combine        -- merges the split partials through their LSE into
+ *                         out/lse and writes out = 0, lse = -inf for tokens that
+ *                         see no key.  Must follow mla_decode_splitkv on the
+ *                         same stream with the same p, sched and workspace.
+ * mla_decode == mla_decode_splitkv followed by mla_combine.
+ */
+int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorbed, const void* q_rope,
+                           const void* kv_pages, const int32_t* block_table, const int32_t* cache_seqlens, float scale,
+                           void* out, float* lse, const void* sched, void* workspace, void* stream);
+int32_t mla_combine(const mla_decode_params* p, void* out, float* lse, const void* sched, void* workspace,
+                    void* stream);
+
+/*
+ * Host-side twin of the split planner (the same code the scheduler kernel runs),
+ * for tests and capacity planning.  cache_seqlens and sched are HOST pointers;
+ * num_units must be >= 1; sched must hold sched_bytes for that unit count.
+ * Layout of sched (int32): [0] = 0x4D4C4131, [1] = units, [2] = B*s_q query blocks,
+ * [3] = partial slots used, [4..7] = 0; then per unit 8 ints {qb_begin, tile_begin,
+ * qb_end, tile_end (exclusive), first_split, 0, 0, 0} (qb_begin = -1: no work); then
+ * num_splits[B*s_q]; then split_offset[B*s_q].  A query block qb = b*s_q + t.
+ */
+int32_t mla_plan_host(const mla_decode_params* p, int32_t num_units, const int32_t* cache_seqlens, void* sched);
+
+/* Unit count mla_decode would use for p on the current device (0 -> as many clusters as fit). */
+int32_t mla_resolve_num_units(const mla_decode_params* p, int32_t* num_units);
+
+/*
+ * Device error word of the current device: synchronises the device, writes the
+ * word to *word (MLA_OK if none; MLA_ERR_TIMEOUT + 16 * site otherwise) and,
+ * if clear != 0, resets it.  Host pointer.
+ */
+int32_t mla_device_error(int32_t* word, int32_t clear);
+
+/*
+ * Failure-path self test: launches one CTA whose bounded wait on a barrier that
+ * nothing completes runs out after timeout_us, sets the device error word and
+ * returns normally.  The GPU context stays usable.  Read the result with
+ * mla_device_error().
+ */
+int32_t mla_wait_selftest(int32_t timeout_us, void* stream);
+
+/* Human-readable name of a status (static string). */
+const char* mla_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H */

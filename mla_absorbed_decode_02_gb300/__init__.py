@@ -1,0 +1,12 @@
+"""GB300 (sm_103a) weight-absorbed MLA decode.
+
+The compute lives in ``libmla_decode.so`` (hand-written CUDA, C ABI declared in
+``include/mla_decode.h``); ``_lib`` is a thin ctypes binding with the same names.
+Importing this package does not load the library; the first call does, and it
+raises if the library has not been built.
+"""
+from ._lib import (  # noqa: F401
+    MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_OUT_BF16, MLA_OUT_F32, MlaError, MlaDecodeParams, Decoder,
+    mla_combine, mla_decode, mla_decode_splitkv, mla_device_error, mla_get_scheduler_metadata, mla_get_workspace_size, mla_plan_host,
+    mla_resolve_num_units, mla_status_string, mla_wait_selftest, library_path, load_library,
+)

@@ -1,0 +1,87 @@
+// Shared device-side pieces of the decode library: the per-device error word,
+// bounded waits, and the kernel argument block.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "plan.h"
+#include "ptx.cuh"
+
+namespace mla {
+
+// First error seen by any kernel of this library on this device (0 = none).
+// Encoding: MLA_ERR_TIMEOUT (4) + 16 * wait site.
+__device__ int g_mla_error = 0;
+
+enum WaitSite : int {
+  kSiteQEmpty = 1, kSiteKvEmpty, kSiteQFull, kSiteKvFull, kSiteSEmpty, kSitePFull, kSiteSFull,
+  kSiteXFree, kSiteXFull, kSitePEmpty, kSiteDrain, kSiteSelftest,
+};
+
+struct WaitCtx {
+  volatile int* abort_local;   // this CTA's abort flag (shared memory)
+  uint32_t abort_peer;         // the peer CTA's abort flag (shared::cluster address), 0 if none
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void raise_abort(const WaitCtx& w, int site) {
+  atomicCAS(&g_mla_error, 0, 4 + 16 * site);
+  *w.abort_local = 1;
+  if (w.abort_peer) asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(w.abort_peer), "r"(1) : "memory");
+}
+
+// Bounded wait by one thread.  Returns false if the CTA is aborting or the wait
+// ran out (then it raises the abort for this CTA and its peer).
+template <bool kClusterScope = false>
+__device__ __noinline__ bool wait_one(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
+  auto poll = [&]() { return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (poll()) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (poll()) return true;
+    if ((i & 31) == 0) {
+      if (*w.abort_local) return false;
+      if (globaltimer_ns() - t0 > w.timeout_ns) {
+        raise_abort(w, site);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait by a whole warp; the result is the same in every lane.
+template <bool kClusterScope = false>
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
+  bool ok = wait_one<kClusterScope>(bar, parity, w, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// After an abort: give in-flight asynchronous copies and MMAs time to land
+// before shared memory and tensor memory are released.
+__device__ __forceinline__ void drain_delay(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) {
+  }
+}
+
+struct DecodeArgs {
+  CUtensorMap map_qr;    // q^R half: bf16 {64, H, NQB}, box {32, 128, 1}, 64-byte swizzle
+  CUtensorMap map_kvc;   // latent of 64 cache rows: box {64 dims, 64 rows}, 128-byte swizzle
+  CUtensorMap map_kvr;   // RoPE key of 64 cache rows: box {32 dims, 64 rows}, 64-byte swizzle
+  const void* q_nope;    // absorbed queries, bf16 [NQB][H][512] (read by threads into tensor memory)
+  const int32_t* block_table;
+  const int32_t* seqlens;
+  const int32_t* sched;
+  void* out;
+  float* lse;
+  float* o_acc;          // split partials [slots][H][512], normalised
+  float* lse_acc;        // [slots][H]
+  float scale_log2;      // softmax scale * log2(e)
+  int32_t H, s_q, causal, max_pages, out_f32, num_units, num_qb;
+  uint64_t timeout_ns;
+};
+
+}  // namespace mla

@@ -1,0 +1,353 @@
+// libmla_decode.so: C ABI (include/mla_decode.h) and the small kernels around
+// the decode kernel -- split planning, LSE combine, bounded-wait self test.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mla_decode.h"
+#include "decode_kernel.cuh"
+
+namespace mla {
+
+// ----------------------------------------------------------------- split planner (device twin)
+__global__ void mla_sched_kernel(const int32_t* seqlens, int B, int s_q, int causal, int U, int32_t* sched) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) plan_units(seqlens, B, s_q, causal, U, sched);
+}
+
+// ----------------------------------------------------------------- LSE combine of split partials
+// out = sum_i exp(lse_i - lse) * out_i, lse = M + ln sum_i exp(lse_i - M), M = max_i lse_i
+// (the merge of split-KV partial results, "MLA inference: two computation paths and
+// FlashMLA", section "Decode attention becomes a compute problem").  Query blocks that see
+// no key get out = 0, lse = -inf.  One CTA of 128 threads per (query block, head).
+__global__ void __launch_bounds__(128) mla_combine_kernel(const int32_t* sched, int U, int NQB, int H,
+                                                          const float* o_acc, const float* lse_acc, void* out,
+                                                          float* lse, int out_f32) {
+  const int qb = blockIdx.x, h = blockIdx.y, d = threadIdx.x * 4;
+  const int32_t* num_splits = sched + kSchedHeader + kUnitInts * U;
+  const int32_t* split_offset = num_splits + NQB;
+  const int ns = num_splits[qb];
+  if (ns == 1) return;
+  const int64_t row = (int64_t)qb * H + h;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float L = -INFINITY;
+  if (ns > 1) {
+    const int off = split_offset[qb];
+    float M = -INFINITY;
+    for (int i = 0; i < ns; ++i) M = fmaxf(M, lse_acc[(int64_t)(off + i) * H + h]);
+    float S = 0.f;
+    for (int i = 0; i < ns; ++i) S += expf(lse_acc[(int64_t)(off + i) * H + h] - M);
+    L = M + logf(S);
+    for (int i = 0; i < ns; ++i) {
+      const float wgt = expf(lse_acc[(int64_t)(off + i) * H + h] - L);
+      const float4 v = *reinterpret_cast<const float4*>(o_acc + ((int64_t)(off + i) * H + h) * 512 + d);
+      acc[0] += wgt * v.x;
+      acc[1] += wgt * v.y;
+      acc[2] += wgt * v.z;
+      acc[3] += wgt * v.w;
+    }
+  }
+  if (out_f32) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + row * 512 + d) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  } else {
+    uint2 o;
+    o.x = pack_bf16(acc[0], acc[1]);
+    o.y = pack_bf16(acc[2], acc[3]);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + row * 512 + d) = o;
+  }
+  if (threadIdx.x == 0) lse[row] = L;
+}
+
+// ----------------------------------------------------------------- bounded-wait self test
+// One CTA waits on a barrier that nothing ever completes; the bounded wait runs
+// out, records MLA_ERR_TIMEOUT in the device error word and the kernel returns.
+__global__ void mla_wait_selftest_kernel(uint64_t timeout_ns) {
+  __shared__ uint64_t barrier_word;
+  __shared__ int abort_word;
+  const uint32_t b = smem_addr(&barrier_word);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    abort_word = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  WaitCtx w;
+  w.abort_local = &abort_word;
+  w.abort_peer = 0;
+  w.timeout_ns = timeout_ns;
+  wait_warp(b, 0, w, kSiteSelftest);
+}
+
+}  // namespace mla
+
+// =================================================================== host side
+namespace {
+
+using namespace mla;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sm_count = 0;
+  int max_clusters = 0;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int32_t device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaFuncSetAttribute(mla_decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+        cudaSuccess)
+      return MLA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (d.sm_count / 2), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (void*)mla_decode_bf16_kernel, &cfg) != cudaSuccess || n <= 0)
+      n = d.sm_count / 2;
+    d.max_clusters = n;
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return MLA_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return MLA_OK;
+}
+
+int32_t check_params(const mla_decode_params* p) {
+  if (!p) return MLA_ERR_INVALID_ARG;
+  if (p->batch < 1 || p->num_heads < 1 || p->num_pages < 1 || p->max_pages_per_seq < 1) return MLA_ERR_INVALID_ARG;
+  if (p->s_q < 1 || p->page_size < 1 || p->num_units < 0 || p->timeout_us < 0) return MLA_ERR_INVALID_ARG;
+  for (int i = 0; i < 5; ++i)
+    if (p->reserved[i] != 0) return MLA_ERR_INVALID_ARG;
+  if (p->kv_dtype != MLA_KV_BF16 && p->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (p->out_dtype != MLA_OUT_BF16 && p->out_dtype != MLA_OUT_F32) return MLA_ERR_INVALID_ARG;
+  if (p->page_size != 64 || p->s_q > 2 || p->num_heads > 128) return MLA_ERR_UNSUPPORTED;
+  if ((int64_t)p->batch * p->s_q > (1 << 24) || (int64_t)p->num_pages * 64 > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+int32_t resolve_units(const mla_decode_params* p, int32_t* U) {
+  if (p->num_units > 0) {
+    *U = p->num_units;
+    return MLA_OK;
+  }
+  DeviceInfo* d = nullptr;
+  int32_t st = device_info(&d);
+  if (st != MLA_OK) return st;
+  *U = d->max_clusters;
+  return MLA_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int32_t encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, const uint64_t* dims,
+                   const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle sw) {
+  cuuint64_t gd[3];
+  cuuint64_t gs[2];
+  cuuint32_t bx[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+  }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+  CUresult r = g_encode(m, dt, rank, const_cast<void*>(ptr), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(int32_t s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+int32_t mla_resolve_num_units(const mla_decode_params* p, int32_t* num_units) {
+  int32_t st = check_params(p);
+  if (st != MLA_OK) return st;
+  if (!num_units) return MLA_ERR_INVALID_ARG;
+  return resolve_units(p, num_units);
+}
+
+int32_t mla_get_workspace_size(const mla_decode_params* p, size_t* sched_bytes, size_t* workspace_bytes) {
+  int32_t st = check_params(p);
+  if (st != MLA_OK) return st;
+  if (!sched_bytes || !workspace_bytes) return MLA_ERR_INVALID_ARG;
+  int32_t U = 0;
+  if ((st = resolve_units(p, &U)) != MLA_OK) return st;
+  const int64_t nqb = (int64_t)p->batch * p->s_q;
+  *sched_bytes = sizeof(int32_t) * (size_t)sched_ints(U, (int)nqb);
+  const size_t slots = (size_t)(nqb + U);
+  *workspace_bytes = align256(slots * p->num_heads * 512 * sizeof(float)) + align256(slots * p->num_heads * sizeof(float));
+  return MLA_OK;
+}
+
+int32_t mla_plan_host(const mla_decode_params* p, int32_t num_units, const int32_t* cache_seqlens, void* sched) {
+  int32_t st = check_params(p);
+  if (st != MLA_OK) return st;
+  if (num_units < 1 || !cache_seqlens || !sched) return MLA_ERR_INVALID_ARG;
+  plan_units(cache_seqlens, p->batch, p->s_q, p->causal != 0, num_units, static_cast<int32_t*>(sched));
+  return MLA_OK;
+}
+
+int32_t mla_get_scheduler_metadata(const mla_decode_params* p, const int32_t* cache_seqlens, void* sched,
+                                   void* stream) {
+  int32_t st = check_params(p);
+  if (st != MLA_OK) return st;
+  if (!cache_seqlens || !sched) return MLA_ERR_INVALID_ARG;
+  int32_t U = 0;
+  if ((st = resolve_units(p, &U)) != MLA_OK) return st;
+  mla_sched_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(cache_seqlens, p->batch, p->s_q,
+                                                                      p->causal != 0, U, static_cast<int32_t*>(sched));
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorbed, const void* q_rope,
+                           const void* kv_pages, const int32_t* block_table, const int32_t* cache_seqlens, float scale,
+                           void* out, float* lse, const void* sched, void* workspace, void* stream) {
+  int32_t st = check_params(p);
+  if (st != MLA_OK) return st;
+  const void* ptrs[] = {q_nope_absorbed, q_rope, kv_pages, block_table, cache_seqlens, out, lse, sched, workspace};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return MLA_ERR_INVALID_ARG;
+  if (p->kv_dtype != MLA_KV_BF16) return MLA_ERR_UNSUPPORTED;
+  DeviceInfo* dinfo = nullptr;
+  if ((st = device_info(&dinfo)) != MLA_OK) return st;
+  int32_t U = 0;
+  if ((st = resolve_units(p, &U)) != MLA_OK) return st;
+  const int H = p->num_heads, NQB = p->batch * p->s_q;
+  const size_t slots = (size_t)NQB + U;
+
+  DecodeArgs a;
+  std::memset(&a, 0, sizeof a);
+  {
+    const uint64_t d[3] = {64, (uint64_t)H, (uint64_t)NQB};
+    const uint64_t s[2] = {64 * 2, (uint64_t)H * 64 * 2};
+    const uint32_t bx[3] = {32, 128, 1};
+    if ((st = encode_map(&a.map_qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_rope, d, s, bx, CU_TENSOR_MAP_SWIZZLE_64B)))
+      return st;
+  }
+  {
+    const uint64_t d[2] = {576, (uint64_t)p->num_pages * 64};
+    const uint64_t s[1] = {576 * 2};
+    const uint32_t bc[2] = {64, 64}, br[2] = {32, 64};
+    if ((st = encode_map(&a.map_kvc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_pages, d, s, bc,
+                         CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+    if ((st = encode_map(&a.map_kvr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_pages, d, s, br,
+                         CU_TENSOR_MAP_SWIZZLE_64B)))
+      return st;
+  }
+  a.q_nope = q_nope_absorbed;
+  a.block_table = block_table;
+  a.seqlens = cache_seqlens;
+  a.sched = static_cast<const int32_t*>(sched);
+  a.out = out;
+  a.lse = lse;
+  a.o_acc = static_cast<float*>(workspace);
+  a.lse_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(slots * H * 512 * sizeof(float)));
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.H = H;
+  a.s_q = p->s_q;
+  a.causal = p->causal != 0;
+  a.max_pages = p->max_pages_per_seq;
+  a.out_f32 = p->out_dtype == MLA_OUT_F32;
+  a.num_units = U;
+  a.num_qb = NQB;
+  a.timeout_ns = (uint64_t)(p->timeout_us > 0 ? p->timeout_us : 2000000) * 1000ull;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * U, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cfg.numAttrs = 0;  // cluster shape comes from __cluster_dims__
+  return cudaLaunchKernelEx(&cfg, mla_decode_bf16_kernel, a) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int32_t mla_combine(const mla_decode_params* p, void* out, float* lse, const void* sched, void* workspace,
+                    void* stream) {
+  int32_t st = check_params(p);
+  if (st != MLA_OK) return st;
+  const void* ptrs[] = {out, lse, sched, workspace};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return MLA_ERR_INVALID_ARG;
+  int32_t U = 0;
+  if ((st = resolve_units(p, &U)) != MLA_OK) return st;
+  const int H = p->num_heads, NQB = p->batch * p->s_q;
+  const size_t slots = (size_t)NQB + U;
+  const float* o_acc = static_cast<const float*>(workspace);
+  const float* lse_acc =
+      reinterpret_cast<const float*>(static_cast<const char*>(workspace) + align256(slots * H * 512 * sizeof(float)));
+  mla_combine_kernel<<<dim3(NQB, H, 1), 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const int32_t*>(sched), U, NQB, H, o_acc, lse_acc, out, lse, p->out_dtype == MLA_OUT_F32);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int32_t mla_decode(const mla_decode_params* p, const void* q_nope_absorbed, const void* q_rope, const void* kv_pages,
+                   const int32_t* block_table, const int32_t* cache_seqlens, float scale, void* out, float* lse,
+                   const void* sched, void* workspace, void* stream) {
+  int32_t st = mla_decode_splitkv(p, q_nope_absorbed, q_rope, kv_pages, block_table, cache_seqlens, scale, out, lse,
+                                  sched, workspace, stream);
+  if (st != MLA_OK) return st;
+  return mla_combine(p, out, lse, sched, workspace, stream);
+}
+
+int32_t mla_device_error(int32_t* word, int32_t clear) {
+  if (!word) return MLA_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_mla_error, sizeof v) != cudaSuccess) return MLA_ERR_CUDA;
+  *word = v;
+  if (clear) {
+    int z = 0;
+    if (cudaMemcpyToSymbol(g_mla_error, &z, sizeof z) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+int32_t mla_wait_selftest(int32_t timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 10000000) return MLA_ERR_INVALID_ARG;
+  mla_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>((uint64_t)timeout_us * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,184 @@
+"""Host-side tests of the C ABI (no GPU needed): the library builds, loads and
+exports every entry point the header declares; argument checks; and the split
+planner (the same code the scheduler kernel runs) covers the work exactly once."""
+import re
+
+import numpy as np
+import pytest
+
+from mla_absorbed_decode_02_gb300 import _lib
+from mla_absorbed_decode_02_gb300.build import build
+from mla_absorbed_decode_02_gb300._lib import MlaDecodeParams
+
+import os
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return _lib.load_library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "mla_decode.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "mla_decode" in names and "mla_get_scheduler_metadata" in names and len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert _lib.mla_status_string(0) == "MLA_OK"
+    assert _lib.mla_status_string(4) == "MLA_ERR_TIMEOUT"
+    assert _lib.mla_status_string(99) == "MLA_ERR_UNKNOWN"
+
+
+def _p(**kw):
+    base = dict(batch=2, s_q=1, num_heads=128, num_pages=10, max_pages_per_seq=5, num_units=4)
+    base.update(kw)
+    return MlaDecodeParams.make(**base)
+
+
+def test_workspace_size_without_gpu(lib):
+    sb, wb = _lib.mla_get_workspace_size(_p(batch=3, s_q=2, num_units=7))
+    assert sb == 4 * (8 + 8 * 7 + 2 * 6)
+    slots = 6 + 7
+    assert wb >= slots * 128 * 512 * 4 + slots * 128 * 4
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(batch=0), _lib.MLA_ERR_INVALID_ARG),
+    (dict(num_heads=129), _lib.MLA_ERR_UNSUPPORTED),
+    (dict(s_q=3), _lib.MLA_ERR_UNSUPPORTED),
+    (dict(page_size=32), _lib.MLA_ERR_UNSUPPORTED),
+    (dict(kv_dtype=7), _lib.MLA_ERR_INVALID_ARG),
+    (dict(out_dtype=5), _lib.MLA_ERR_INVALID_ARG),
+    (dict(num_units=-1), _lib.MLA_ERR_INVALID_ARG),
+])
+def test_bad_params_are_rejected(lib, kw, status):
+    with pytest.raises(_lib.MlaError) as e:
+        _lib.mla_get_workspace_size(_p(**kw))
+    assert e.value.status == status
+
+
+def test_null_pointers_rejected_before_any_launch(lib):
+    with pytest.raises(_lib.MlaError) as e:
+        _lib.mla_decode(_p(), None, None, None, None, None, 0.07, None, None, None, None, stream=0)
+    assert e.value.status == _lib.MLA_ERR_INVALID_ARG
+
+
+def test_reserved_must_be_zero(lib):
+    p = _p()
+    p.reserved[2] = 1
+    with pytest.raises(_lib.MlaError):
+        _lib.mla_get_workspace_size(p)
+
+
+# ------------------------------------------------------------------ split planner
+
+TILE = 128
+FIX = 1
+
+
+def visible(L, s_q, t, causal):
+    n = L - s_q + 1 + t if causal else L
+    return max(0, min(n, L))
+
+
+def decode_plan(sched, B, s_q, causal, seqlens):
+    """Expand the metadata into the list of pieces (unit, qb, t0, t1, split_idx)."""
+    U, nqb = sched[1], sched[2]
+    assert sched[0] == _lib.SCHED_MAGIC and nqb == B * s_q
+    units = sched[8:8 + 8 * U].reshape(U, 8)
+    num_splits = sched[8 + 8 * U:8 + 8 * U + nqb]
+    offsets = sched[8 + 8 * U + nqb:]
+    ntiles = [-(-visible(seqlens[q // s_q], s_q, q % s_q, causal) // TILE) for q in range(nqb)]
+    pieces = []
+    for u in range(U):
+        qb0, tb, qb1, te, fs = units[u, :5]
+        if qb0 < 0:
+            continue
+        for qb in range(qb0, qb1 + 1):
+            a = tb if qb == qb0 else 0
+            b = te if qb == qb1 else ntiles[qb]
+            if ntiles[qb] > 0 and a < b:
+                pieces.append((u, qb, a, b, fs if qb == qb0 else 0))
+    return pieces, ntiles, num_splits, offsets
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_plan_covers_every_tile_once(lib, seed):
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 80))
+    s_q = int(rng.integers(1, 3))
+    causal = bool(rng.integers(0, 2))
+    kind = seed % 4
+    if kind == 0:
+        seqlens = rng.integers(0, 3000, size=B)
+    elif kind == 1:
+        seqlens = np.full(B, int(rng.integers(1, 9000)))
+    elif kind == 2:
+        seqlens = np.round(np.exp(rng.uniform(np.log(1), np.log(140000), size=B)))
+    else:
+        seqlens = rng.choice([0, 1, 2, 127, 128, 129, 65536], size=B)
+    seqlens = seqlens.astype(np.int32)
+    U = int(rng.integers(1, 100))
+    p = MlaDecodeParams.make(B, s_q, 128, 100, 10, causal=causal, num_units=U)
+    sched = _lib.mla_plan_host(p, U, seqlens)
+    pieces, ntiles, num_splits, offsets = decode_plan(sched, B, s_q, causal, seqlens)
+    # every tile of every query block exactly once, pieces non-empty
+    seen = {}
+    for u, qb, a, b, si in pieces:
+        assert b > a
+        for t in range(a, b):
+            assert (qb, t) not in seen
+            seen[(qb, t)] = u
+    assert len(seen) == sum(ntiles)
+    # units hold contiguous, increasing stretches of (qb, tile)
+    order = [(qb, a) for _, qb, a, _, _ in pieces]
+    assert order == sorted(order)
+    # split bookkeeping: split indices 0..n-1 per query block, slots disjoint
+    per_qb = {}
+    for u, qb, a, b, si in pieces:
+        per_qb.setdefault(qb, []).append(si)
+    slots = set()
+    for qb in range(B * s_q):
+        got = per_qb.get(qb, [])
+        assert num_splits[qb] == len(got)
+        assert sorted(got) == list(range(len(got)))
+        if len(got) > 1:
+            for i in range(len(got)):
+                s = offsets[qb] + i
+                assert s not in slots
+                slots.add(s)
+    assert sched[3] == len(slots) <= B * s_q + U
+
+
+def test_plan_balances_load(lib):
+    seqlens = np.full(32, 4096, np.int32)
+    U = 76
+    p = MlaDecodeParams.make(32, 1, 128, 2048, 64, num_units=U)
+    sched = _lib.mla_plan_host(p, U, seqlens)
+    pieces, ntiles, _, _ = decode_plan(sched, 32, 1, True, seqlens)
+    load = np.zeros(U)
+    for u, qb, a, b, _ in pieces:
+        load[u] += (b - a) + FIX
+    total = sum(ntiles) + FIX * 32
+    assert load.max() == sched[4] <= -(-total // U) + 2 * FIX
+    assert (load > 0).sum() >= U - 2
+
+
+def test_plan_handles_empty_sequences(lib):
+    seqlens = np.array([0, 5, 0, 0, 300, 0], np.int32)
+    p = MlaDecodeParams.make(6, 1, 128, 10, 5, num_units=3)
+    sched = _lib.mla_plan_host(p, 3, seqlens)
+    pieces, ntiles, num_splits, _ = decode_plan(sched, 6, 1, True, seqlens)
+    assert [num_splits[i] for i in (0, 2, 3, 5)] == [0, 0, 0, 0]
+    assert sum(b - a for _, _, a, b, _ in pieces) == sum(ntiles) == 1 + 3

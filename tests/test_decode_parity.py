@@ -1,0 +1,171 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle.
+
+Small cases compare every output element; the full-size benchmark workloads
+compare sampled (sequence, head) rows the oracle computes one by one, in the
+same launch configuration the benchmark times (default unit count)."""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import mla_workloads as mw
+from gpu_util import BF16_TOL, compare, oracle_full, oracle_sampled, run_gpu, to_device, params_for
+
+pytestmark = pytest.mark.gpu
+
+THREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_absorbed_decode_02_gb300.build import build
+    build()
+
+
+def full_check(w, tol=BF16_TOL, num_units=0, what=""):
+    out, lse, _ = run_gpu(w, num_units=num_units)
+    ref_out, ref_lse = oracle_full(w, threads=THREADS)
+    return compare(out, lse, ref_out, ref_lse, tol, what or w.name, out_bf16=w.out_dtype == "bf16")
+
+
+# ------------------------------------------------------------------ the benchmark workloads
+
+def test_workload_tiny_full():
+    w = mw.make_workload(0)
+    errs = full_check(w)
+    print("tiny", errs)
+
+
+@pytest.mark.parametrize("index", [1, 2, 3])
+def test_workload_full_size_sampled(index):
+    w = mw.make_workload(index)
+    out, lse, _ = run_gpu(w)
+    rng = np.random.default_rng(1000 + index)
+    items = []
+    for b in range(w.batch):
+        for t in range(w.s_q):
+            heads = sorted(rng.choice(w.num_heads, size=3, replace=False).tolist())
+            items.append((b, t, heads))
+    ref = oracle_sampled(w, items, threads=THREADS)
+    got_o, got_l, ref_o, ref_l = [], [], [], []
+    for (b, t), (heads, o, l) in ref.items():
+        got_o.append(out[b, t, heads])
+        got_l.append(lse[b, t, heads])
+        ref_o.append(o)
+        ref_l.append(l)
+    errs = compare(np.concatenate(got_o), np.concatenate(got_l), np.concatenate(ref_o), np.concatenate(ref_l),
+                   BF16_TOL, w.name, out_bf16=True)
+    print(w.name, errs)
+
+
+# ------------------------------------------------------------------ ragged tails, splits, head counts
+
+@pytest.mark.parametrize("num_units", [0, 1, 3, 7])
+def test_ragged_lengths_and_splits(num_units):
+    lens = [1, 63, 64, 65, 127, 128, 129, 255, 256, 257, 1000, 2049]
+    w = mw.make_custom(lens, num_heads=128, seed=11, pool_factor=1.3)
+    full_check(w, num_units=num_units, what=f"ragged U={num_units}")
+
+
+@pytest.mark.parametrize("H", [1, 16, 17, 100, 128])
+def test_head_counts(H):
+    w = mw.make_custom([130, 7, 700], num_heads=H, seed=12)
+    full_check(w, num_units=2, what=f"H={H}")
+
+
+def test_f32_output():
+    w = mw.make_custom([200, 513], num_heads=64, out_dtype="f32", seed=13)
+    full_check(w, num_units=3)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_two_new_tokens(causal):
+    w = mw.make_custom([2, 3, 128, 129, 600], num_heads=128, s_q=2, causal=causal, seed=14)
+    full_check(w, num_units=4, what=f"s_q=2 causal={causal}")
+
+
+def test_empty_sequences():
+    w = mw.make_custom([0, 100, 0, 1], num_heads=32, seed=15)
+    out, lse, _ = run_gpu(w, num_units=2)
+    ref_out, ref_lse = oracle_full(w)
+    compare(out, lse, ref_out, ref_lse, BF16_TOL, "empty", out_bf16=True)
+    assert np.all(lse[0] == -np.inf) and np.all(out[0] == 0) and np.all(lse[2] == -np.inf)
+
+
+def test_all_pages_alias_one_physical_page():
+    w = mw.make_custom([300, 64, 129], num_heads=128, seed=16)
+    w.block_table[w.block_table >= 0] = 0
+    full_check(w, num_units=3, what="aliased pages")
+
+
+def test_zero_query_gives_uniform_average():
+    w = mw.make_custom([1000, 77], num_heads=128, seed=17)
+    w.q_nope[:] = 0
+    w.q_rope[:] = 0
+    errs = full_check(w, num_units=2, what="uniform")
+    out, lse, _ = run_gpu(w, num_units=2)
+    np.testing.assert_allclose(lse[:, 0, 0], np.log(w.seqlens), rtol=0, atol=1e-4)
+
+
+def test_dominant_key():
+    w = mw.make_custom([500, 300], num_heads=128, seed=18)
+    # give key 123 of sequence 0 a RoPE key aligned with every head's RoPE query: it dominates
+    page = w.block_table[0, 123 // 64]
+    qr = w.q_rope.view(np.uint16)
+    kr = (qr[0, 0].astype(np.uint32) << 16).view(np.float32).sum(axis=0)   # sum over heads
+    big = np.sign(kr) * 8.0
+    w.kv[page, 123 % 64, 512:] = mw.to_bf16_bits(big.astype(np.float32))
+    full_check(w, num_units=2, what="dominant key")
+
+
+def test_long_tail_row_garbage_is_ignored():
+    """Cache rows past the sequence end inside the last page hold NaN: they must not leak."""
+    w = mw.make_custom([65, 130, 1], num_heads=128, seed=19)
+    nan_bf16 = np.uint16(0x7FC0)
+    for b, L in enumerate(w.seqlens):
+        last = (int(L) - 1) // 64
+        page = w.block_table[b, last]
+        w.kv[page, int(L) % 64 or 64:, :] = nan_bf16
+    full_check(w, num_units=2, what="NaN past the end")
+
+
+# ------------------------------------------------------------------ metadata, errors
+
+def test_device_plan_matches_host_plan():
+    import torch
+    from mla_absorbed_decode_02_gb300 import Decoder, mla_plan_host
+    w = mw.make_workload(2)
+    _, _, _, _, seq = to_device(w)
+    dec = Decoder(params_for(w))
+    dec.plan(seq)
+    torch.cuda.synchronize()
+    host = mla_plan_host(params_for(w, num_units=dec.num_units), dec.num_units, w.seqlens)
+    assert np.array_equal(dec.sched.cpu().numpy(), host)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    import torch
+    from mla_absorbed_decode_02_gb300 import mla_wait_selftest, mla_device_error
+    mla_device_error(clear=True)
+    mla_wait_selftest(20000)
+    word = mla_device_error(clear=True)
+    assert word % 16 == 4 and word // 16 > 0
+    # the context is still usable afterwards
+    x = torch.arange(10, device="cuda").sum().item()
+    assert x == 45
+    assert mla_device_error(clear=True) == 0
+
+
+def test_unaligned_pointer_rejected():
+    import torch
+    from mla_absorbed_decode_02_gb300 import MlaError, mla_decode
+    w = mw.make_custom([10], num_heads=16, seed=20)
+    q_nope, q_rope, kv, bt, seq = to_device(w)
+    p = params_for(w, num_units=1)
+    buf = torch.empty(100000, dtype=torch.uint8, device="cuda")
+    with pytest.raises(MlaError):
+        mla_decode(p, q_nope, q_rope, kv, bt, seq, w.scale, buf[1:], buf, buf, buf)
