@@ -328,7 +328,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_dec
     while (ok && have) {
       const int b = pc.qb / args.s_q;
       const int vis = visible_keys(args.seqlens[b], args.s_q, pc.qb % args.s_q, args.causal);
-      float m_used = -INFINITY, l = 0.f;
+      float m_used = -INFINITY, l = 0.f, lq = 0.f;  // l: exact row sum (for lse); lq: sum of the bf16 weights (for O)
       const int n = pc.t1 - pc.t0;
       Piece nxt;
       bool have_next = false;
@@ -419,15 +419,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_dec
         const float alpha = resc ? exp2f(m_used - m_new) : 1.f;
         m_used = m_new;
         uint32_t pk[64];
-        float rs = 0.f;
+        float rs = 0.f, rq = 0.f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          pk[j] = pack_bf16(exp2f(s[2 * j] - m_new), exp2f(s[2 * j + 1] - m_new));
-          // the row sum uses the bf16 weights the PV product sees, so the output is an
-          // exact convex combination of the values
-          rs += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xFFFF0000u);
+          const float p0 = exp2f(s[2 * j] - m_new), p1 = exp2f(s[2 * j + 1] - m_new);
+          pk[j] = pack_bf16(p0, p1);
+          rs += p0 + p1;
+          // O is normalised by the sum of the bf16 weights the PV product saw, so the output
+          // is an exact convex combination of the values
+          rq += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xFFFF0000u);
         }
         l = l * alpha + rs;
+        lq = lq * alpha + rq;
         // ---- previous PV done: P buffer, O and the stage are ours
         if (p_it > 0 && !(ok = wait_warp(bar(B_PV_DONE), (p_it - 1) & 1, wc, kSitePEmpty))) break;
         tc_fence_after();
@@ -474,7 +477,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_dec
       tc_fence_after();
       const bool split = num_splits[pc.qb] > 1;
       const int slot = split ? split_offset[pc.qb] + pc.split : 0;
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lq;
       const bool write_row = r < H;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
