@@ -16,8 +16,23 @@
 namespace mla {
 
 // ----------------------------------------------------------------- split planner (device twin)
-__global__ void mla_sched_kernel(const int32_t* seqlens, int B, int s_q, int causal, int U, int32_t* sched) {
-  if (threadIdx.x == 0 && blockIdx.x == 0) plan_units(seqlens, B, s_q, causal, U, sched);
+// One CTA of 1024 threads runs the planner phases of plan.h (the prefix sums on one thread).
+__global__ void __launch_bounds__(1024) mla_sched_kernel(const int32_t* seqlens, int B, int s_q, int causal, int U,
+                                                         int32_t* sched) {
+  __shared__ int64_t sh_total;
+  const int NQB = B * s_q, tid = threadIdx.x, nt = blockDim.x;
+  int32_t* units = sched + kSchedHeader;
+  int32_t* num_splits = units + kUnitInts * U;
+  int32_t* pos = num_splits + NQB;  // scratch until the last phase
+  plan_phase_cost(seqlens, s_q, causal, NQB, pos, tid, nt);
+  __syncthreads();
+  if (tid == 0) sh_total = plan_phase_scan(pos, NQB);
+  __syncthreads();
+  const int64_t total = sh_total, Bq = plan_budget(total, U);
+  plan_phase_units(seqlens, s_q, causal, NQB, pos, total, Bq, U, units, tid, nt);
+  plan_phase_splits(seqlens, s_q, causal, NQB, pos, Bq, num_splits, tid, nt);
+  __syncthreads();
+  if (tid == 0) plan_phase_finish(NQB, U, Bq, sched);
 }
 
 // ----------------------------------------------------------------- LSE combine of split partials
@@ -234,7 +249,7 @@ int32_t mla_get_scheduler_metadata(const mla_decode_params* p, const int32_t* ca
   if (!cache_seqlens || !sched) return MLA_ERR_INVALID_ARG;
   int32_t U = 0;
   if ((st = resolve_units(p, &U)) != MLA_OK) return st;
-  mla_sched_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(cache_seqlens, p->batch, p->s_q,
+  mla_sched_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(cache_seqlens, p->batch, p->s_q,
                                                                       p->causal != 0, U, static_cast<int32_t*>(sched));
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

@@ -23,10 +23,11 @@ namespace mla {
 constexpr int32_t kSchedMagic = 0x4D4C4131;  // "MLA1"
 constexpr int kSchedHeader = 8;               // int32 header words
 constexpr int kUnitInts = 8;                  // int32 words per unit record
-constexpr int kTile = 128;                    // tokens per work tile (two 64-token pages)
+constexpr int kTile = 64;                     // tokens per work tile (one page)
 // Cost of one piece of work beyond its tiles, in tile units: loading the
-// query half and writing the 128 x 256 output half (about one tile of bytes).
-constexpr int kPieceFixedCost = 1;
+// 128 x 288 query half and writing the 128 x 256 output half (about two
+// tiles' worth of bytes, mostly served by L2).
+constexpr int kPieceFixedCost = 2;
 
 MLA_HD inline int32_t visible_keys(int32_t L, int s_q, int t, int causal) {
   int32_t n = causal ? L - s_q + 1 + t : L;
@@ -41,80 +42,102 @@ MLA_HD inline int64_t sched_ints(int num_units, int num_qb) {
   return kSchedHeader + (int64_t)kUnitInts * num_units + 2 * (int64_t)num_qb;
 }
 
-// Greedy pass with a per-unit cost budget: walks query blocks in order, filling
-// unit after unit; a piece (one query block's tile range inside one unit) costs
-// its tiles plus kPieceFixedCost.  Returns false if the work needs more than U
-// units.  With write == true it also fills the unit records and num_splits.
-MLA_HD inline bool plan_pass(const int32_t* seqlens, int B, int s_q, int causal, int U, int64_t budget, bool write,
-                             int32_t* units, int32_t* num_splits) {
-  const int NQB = B * s_q;
-  int u = 0;
-  bool unit_used = false;
-  int64_t room = budget;
-  for (int qb = 0; qb < NQB; ++qb) {
+// Work positions.  Query blocks are laid out one after another on a line of
+// cost units: block qb occupies [pos[qb], pos[qb] + kPieceFixedCost + nt[qb]),
+// its first kPieceFixedCost units standing for the per-piece overhead and then
+// one unit per 64-token tile (tile t at pos[qb] + kPieceFixedCost + t).  With
+// B = ceil(total / U), unit u owns the tiles whose positions fall in
+// [u*B, (u+1)*B).  Everything below follows in closed form, so the device runs
+// each phase in parallel (the prefix sums on one thread).
+//
+// Phase 1 (per query block): nt[qb] and cost; written into num_splits[] as scratch.
+MLA_HD inline void plan_phase_cost(const int32_t* seqlens, int s_q, int causal, int NQB, int32_t* cost, int begin,
+                                   int stride) {
+  for (int qb = begin; qb < NQB; qb += stride) {
     const int32_t nt = num_tiles(visible_keys(seqlens[qb / s_q], s_q, qb % s_q, causal));
-    int32_t tile = 0, splits = 0;
-    while (tile < nt) {
-      if (unit_used && room <= kPieceFixedCost) {  // no useful room left: next unit
-        if (++u == U) return false;
-        room = budget;
-        unit_used = false;
-      }
-      int64_t take = nt - tile;
-      if (take > room - kPieceFixedCost) take = room - kPieceFixedCost;
-      if (write) {
-        int32_t* rec = units + kUnitInts * u;
-        if (!unit_used) {
-          rec[0] = qb;
-          rec[1] = tile;
-          rec[4] = splits;
-        }
-        rec[2] = qb;
-        rec[3] = tile + (int32_t)take;
-      }
-      unit_used = true;
-      ++splits;
-      tile += (int32_t)take;
-      room -= take + kPieceFixedCost;
-    }
-    if (write) num_splits[qb] = splits;
+    cost[qb] = nt > 0 ? nt + kPieceFixedCost : 0;
   }
-  return true;
 }
 
-// Fills sched (sched_ints(U, B*s_q) int32 words).  Query block qb = b*s_q + t.
-// Units hold contiguous ranges in (qb, tile) order; every non-empty query block
-// is covered exactly once; a piece never holds zero tiles.  The budget is the
-// smallest per-unit cost with which the greedy pass fits in U units (binary
-// search; feasibility only improves with a larger budget).
-MLA_HD inline void plan_units(const int32_t* seqlens, int B, int s_q, int causal, int U, int32_t* sched) {
-  const int NQB = B * s_q;
-  int32_t* units = sched + kSchedHeader;
-  int32_t* num_splits = units + kUnitInts * U;
-  int32_t* split_offset = num_splits + NQB;
-  for (int u = 0; u < U; ++u) {
+// Phase 2 (one thread): exclusive prefix sum of cost -> pos (in place); returns the total.
+MLA_HD inline int64_t plan_phase_scan(int32_t* cost_to_pos, int NQB) {
+  int64_t acc = 0;
+  for (int qb = 0; qb < NQB; ++qb) {
+    const int64_t c = cost_to_pos[qb];
+    cost_to_pos[qb] = (int32_t)acc;
+    acc += c;
+  }
+  return acc;
+}
+
+MLA_HD inline int64_t plan_budget(int64_t total, int U) {
+  int64_t B = (total + U - 1) / U;
+  return B < 1 ? 1 : B;
+}
+
+// Phase 3 (per unit): the unit record.  pos[] = block start positions.
+MLA_HD inline void plan_phase_units(const int32_t* seqlens, int s_q, int causal, int NQB, const int32_t* pos,
+                                    int64_t total, int64_t B, int U, int32_t* units, int begin, int stride) {
+  for (int u = begin; u < U; u += stride) {
     int32_t* rec = units + kUnitInts * u;
     rec[0] = -1;
     rec[1] = rec[2] = rec[3] = rec[4] = rec[5] = rec[6] = rec[7] = 0;
+    const int64_t lo = (int64_t)u * B, hi = lo + B;  // tile positions [lo, hi)
+    if (lo >= total) continue;
+    // first block whose last tile position >= lo
+    int a = 0, b = NQB;
+    while (a < b) {
+      const int m = (a + b) / 2;
+      const int32_t nt = num_tiles(visible_keys(seqlens[m / s_q], s_q, m % s_q, causal));
+      const int64_t last = (int64_t)pos[m] + kPieceFixedCost + nt - 1;
+      if (nt > 0 && last >= lo) b = m; else if (nt == 0 && (int64_t)pos[m] > lo) b = m; else a = m + 1;
+    }
+    // skip empty blocks
+    int qb0 = a;
+    while (qb0 < NQB && num_tiles(visible_keys(seqlens[qb0 / s_q], s_q, qb0 % s_q, causal)) == 0) ++qb0;
+    if (qb0 >= NQB) continue;
+    const int64_t first0 = (int64_t)pos[qb0] + kPieceFixedCost;
+    if (first0 >= hi) continue;  // the range holds only overhead positions
+    // last block whose first tile position < hi
+    a = qb0;
+    b = NQB;
+    while (b - a > 1) {
+      const int m = (a + b) / 2;
+      if ((int64_t)pos[m] + kPieceFixedCost < hi) a = m; else b = m;
+    }
+    int qb1 = a;
+    while (qb1 > qb0 && num_tiles(visible_keys(seqlens[qb1 / s_q], s_q, qb1 % s_q, causal)) == 0) --qb1;
+    const int32_t nt1 = num_tiles(visible_keys(seqlens[qb1 / s_q], s_q, qb1 % s_q, causal));
+    const int64_t t_begin = lo - first0 > 0 ? lo - first0 : 0;
+    int64_t t_end = hi - ((int64_t)pos[qb1] + kPieceFixedCost);
+    if (t_end > nt1) t_end = nt1;
+    const int64_t fu = first0 / B;  // first unit holding a tile of qb0
+    rec[0] = qb0;
+    rec[1] = (int32_t)t_begin;
+    rec[2] = qb1;
+    rec[3] = (int32_t)t_end;
+    rec[4] = (int32_t)(u - fu);
   }
-  for (int qb = 0; qb < NQB; ++qb) num_splits[qb] = 0;
-  int64_t total = 0;
-  for (int qb = 0; qb < NQB; ++qb) {
-    int32_t nt = num_tiles(visible_keys(seqlens[qb / s_q], s_q, qb % s_q, causal));
-    if (nt > 0) total += nt + kPieceFixedCost;
+}
+
+// Phase 4 (per query block): number of units its tiles span.
+MLA_HD inline void plan_phase_splits(const int32_t* seqlens, int s_q, int causal, int NQB, const int32_t* pos,
+                                     int64_t B, int32_t* num_splits, int begin, int stride) {
+  for (int qb = begin; qb < NQB; qb += stride) {
+    const int32_t nt = num_tiles(visible_keys(seqlens[qb / s_q], s_q, qb % s_q, causal));
+    if (nt == 0) {
+      num_splits[qb] = 0;
+      continue;
+    }
+    const int64_t first = (int64_t)pos[qb] + kPieceFixedCost;
+    num_splits[qb] = (int32_t)((first + nt - 1) / B - first / B + 1);
   }
-  int64_t lo = (total + U - 1) / U;
-  if (lo < kPieceFixedCost + 1) lo = kPieceFixedCost + 1;
-  int64_t hi = total + kPieceFixedCost + 1;  // one unit takes everything
-  if (hi < lo) hi = lo;
-  while (lo < hi) {
-    const int64_t mid = lo + (hi - lo) / 2;
-    if (plan_pass(seqlens, B, s_q, causal, U, mid, false, units, num_splits))
-      hi = mid;
-    else
-      lo = mid + 1;
-  }
-  plan_pass(seqlens, B, s_q, causal, U, lo, true, units, num_splits);
+}
+
+// Phase 5 (one thread): slots of the split partials; header.
+MLA_HD inline void plan_phase_finish(int NQB, int U, int64_t B, int32_t* sched) {
+  int32_t* num_splits = sched + kSchedHeader + kUnitInts * U;
+  int32_t* split_offset = num_splits + NQB;
   int32_t slots = 0;
   for (int qb = 0; qb < NQB; ++qb) {
     split_offset[qb] = slots;
@@ -124,8 +147,23 @@ MLA_HD inline void plan_units(const int32_t* seqlens, int B, int s_q, int causal
   sched[1] = U;
   sched[2] = NQB;
   sched[3] = slots;
-  sched[4] = (int32_t)lo;  // per-unit budget (diagnostic)
+  sched[4] = (int32_t)B;  // per-unit budget of positions (diagnostic)
   sched[5] = sched[6] = sched[7] = 0;
+}
+
+// Host twin: all phases in order, one "thread".  The split_offset region of
+// sched serves as scratch for the block positions until phase 5 fills it.
+MLA_HD inline void plan_units(const int32_t* seqlens, int B_, int s_q, int causal, int U, int32_t* sched) {
+  const int NQB = B_ * s_q;
+  int32_t* units = sched + kSchedHeader;
+  int32_t* num_splits = units + kUnitInts * U;
+  int32_t* pos = num_splits + NQB;
+  plan_phase_cost(seqlens, s_q, causal, NQB, pos, 0, 1);
+  const int64_t total = plan_phase_scan(pos, NQB);
+  const int64_t B = plan_budget(total, U);
+  plan_phase_units(seqlens, s_q, causal, NQB, pos, total, B, U, units, 0, 1);
+  plan_phase_splits(seqlens, s_q, causal, NQB, pos, B, num_splits, 0, 1);
+  plan_phase_finish(NQB, U, B, sched);
 }
 
 }  // namespace mla

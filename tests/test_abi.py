@@ -83,8 +83,8 @@ def test_reserved_must_be_zero(lib):
 
 # ------------------------------------------------------------------ split planner
 
-TILE = 128
-FIX = 1
+TILE = 64
+FIX = 2
 
 
 def visible(L, s_q, t, causal):
@@ -129,7 +129,7 @@ def test_plan_covers_every_tile_once(lib, seed):
     else:
         seqlens = rng.choice([0, 1, 2, 127, 128, 129, 65536], size=B)
     seqlens = seqlens.astype(np.int32)
-    U = int(rng.integers(1, 100))
+    U = int(rng.choice([1, 2, 3, 7, 19, 76, 148, 500]))
     p = MlaDecodeParams.make(B, s_q, 128, 100, 10, causal=causal, num_units=U)
     sched = _lib.mla_plan_host(p, U, seqlens)
     pieces, ntiles, num_splits, offsets = decode_plan(sched, B, s_q, causal, seqlens)
@@ -171,7 +171,9 @@ def test_plan_balances_load(lib):
     for u, qb, a, b, _ in pieces:
         load[u] += (b - a) + FIX
     total = sum(ntiles) + FIX * 32
-    assert load.max() == sched[4] <= -(-total // U) + 2 * FIX
+    budget = -(-total // U)
+    assert sched[4] == budget
+    assert load.max() <= budget + FIX      # one extra piece overhead at most
     assert (load > 0).sum() >= U - 2
 
 
@@ -181,4 +183,4 @@ def test_plan_handles_empty_sequences(lib):
     sched = _lib.mla_plan_host(p, 3, seqlens)
     pieces, ntiles, num_splits, _ = decode_plan(sched, 6, 1, True, seqlens)
     assert [num_splits[i] for i in (0, 2, 3, 5)] == [0, 0, 0, 0]
-    assert sum(b - a for _, _, a, b, _ in pieces) == sum(ntiles) == 1 + 3
+    assert sum(b - a for _, _, a, b, _ in pieces) == sum(ntiles) == -(-5 // TILE) + -(-300 // TILE)
