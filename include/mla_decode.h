@@ -56,6 +56,7 @@ typedef enum {
   MLA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed (no device, launch failure, ...) */
   MLA_ERR_TIMEOUT = 4,      /* device error word: a bounded wait inside a kernel ran out */
   MLA_ERR_WORKSPACE = 5,    /* scheduler metadata does not match the params (wrong unit count or batch) */
+  MLA_ERR_SCRATCH_LIMIT = 6, /* mla_decode_noalloc: the request needs more than MLA_NOALLOC_SCRATCH_BYTES */
 } mla_status;
 
 typedef enum {
@@ -172,6 +173,39 @@ int32_t mla_device_error(int32_t* word, int32_t clear);
  * mla_device_error().
  */
 int32_t mla_wait_selftest(int32_t timeout_us, void* stream);
+
+/*
+ * Allocation-free decode, for callers that cannot call cudaMalloc on their
+ * decode path: serving engines and plugin hosts that reserve all device memory
+ * for their own pool allocator at start-up (a cudaMalloc would take memory from
+ * outside that pool, and cudaMalloc/cudaFree can synchronise the device in the
+ * middle of a step).  The paper has no counterpart; it is an interface of this
+ * library only.
+ *
+ * Same inputs, outputs, rules and results as mla_get_scheduler_metadata
+ * followed by mla_decode with the same p, but the scheduler metadata and the
+ * split partials live in one fixed device array inside the library,
+ * MLA_NOALLOC_SCRATCH_BYTES (64 MiB) per GPU, reserved by the CUDA runtime
+ * when it loads the library's device code on that GPU and held until the
+ * process exits.  It holds
+ * align256(sched_bytes) + workspace_bytes of mla_get_workspace_size: with 128
+ * heads, batch * s_q plus the unit count up to 255.  A larger request returns
+ * MLA_ERR_SCRATCH_LIMIT and launches nothing.  The call itself allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *
+ * The first call on a device also looks up the array's device address for that
+ * device (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.
+ *
+ * Every call on a device shares the one array, which keeps the last call's
+ * contents; nothing in it needs to start at zero.  Calls whose kernels overlap
+ * on the GPU (other streams, other host threads) race on the array and give
+ * undefined results: order them on one stream or with events.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int32_t mla_decode_noalloc(const mla_decode_params* p, const void* q_nope_absorbed, const void* q_rope,
+                           const void* kv_pages, const int32_t* block_table, const int32_t* cache_seqlens,
+                           float scale, void* out, float* lse, void* stream);
 
 /* Human-readable name of a status (static string). */
 const char* mla_status_string(int32_t status);

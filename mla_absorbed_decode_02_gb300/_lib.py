@@ -12,7 +12,9 @@ import threading
 
 import numpy as np
 
-MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_TIMEOUT, MLA_ERR_WORKSPACE = range(6)
+(MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA, MLA_ERR_TIMEOUT, MLA_ERR_WORKSPACE,
+ MLA_ERR_SCRATCH_LIMIT) = range(7)
+MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 MLA_KV_BF16, MLA_KV_FP8_E4M3 = 0, 1
 MLA_OUT_BF16, MLA_OUT_F32 = 0, 1
 SCHED_MAGIC = 0x4D4C4131
@@ -68,6 +70,7 @@ def load_library():
             "mla_resolve_num_units": ([P, ctypes.POINTER(i32)], i32),
             "mla_device_error": ([ctypes.POINTER(i32), i32], i32),
             "mla_wait_selftest": ([i32, vp], i32),
+            "mla_decode_noalloc": ([P, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp], i32),
             "mla_status_string": ([i32], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -80,7 +83,7 @@ def load_library():
 
 def _status_name(status: int) -> str:
     names = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_CUDA",
-             4: "MLA_ERR_TIMEOUT", 5: "MLA_ERR_WORKSPACE"}
+             4: "MLA_ERR_TIMEOUT", 5: "MLA_ERR_WORKSPACE", 6: "MLA_ERR_SCRATCH_LIMIT"}
     return names.get(status, "MLA_ERR_UNKNOWN")
 
 
@@ -152,6 +155,15 @@ def mla_decode_splitkv(p: MlaDecodeParams, q_nope_absorbed, q_rope, kv_pages, bl
 def mla_combine(p: MlaDecodeParams, out, lse, sched, workspace, stream=None):
     _check(load_library().mla_combine(ctypes.byref(p), _ptr(out), _ptr(lse), _ptr(sched), _ptr(workspace),
                                       _stream(stream)), "mla_combine")
+
+
+def mla_decode_noalloc(p: MlaDecodeParams, q_nope_absorbed, q_rope, kv_pages, block_table, cache_seqlens,
+                       scale: float, out, lse, stream=None):
+    """Scheduler metadata + decode with the library's fixed device scratch array
+    instead of caller buffers (for callers that cannot allocate device memory)."""
+    _check(load_library().mla_decode_noalloc(ctypes.byref(p), _ptr(q_nope_absorbed), _ptr(q_rope), _ptr(kv_pages),
+                                             _ptr(block_table), _ptr(cache_seqlens), float(scale), _ptr(out),
+                                             _ptr(lse), _stream(stream)), "mla_decode_noalloc")
 
 
 def mla_device_error(clear: bool = True) -> int:

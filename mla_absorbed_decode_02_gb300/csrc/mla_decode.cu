@@ -210,6 +210,7 @@ const char* mla_status_string(int32_t s) {
     case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
     case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
     case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_SCRATCH_LIMIT: return "MLA_ERR_SCRATCH_LIMIT";
     default: return "MLA_ERR_UNKNOWN";
   }
 }
@@ -366,3 +367,57 @@ int32_t mla_wait_selftest(int32_t timeout_us, void* stream) {
 }
 
 }  // extern "C"
+
+// =================================================================== allocation-free decode
+// For callers that cannot call cudaMalloc on their decode path: serving engines
+// and plugin hosts that reserve all device memory for their own pool allocator
+// at start-up (a cudaMalloc would take memory outside that pool, and
+// cudaMalloc/cudaFree can synchronise the device in the middle of a step).
+// They pass inputs and outputs as usual; the scheduler metadata and the split
+// partials live in this fixed array, which every GPU that loads the library
+// holds until the process exits.
+static __device__ __align__(256) unsigned char g_mla_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+void* g_noalloc_ptr[64];  // device address of g_mla_noalloc_scratch per device (guarded by g_mu)
+
+// Set-up, once per device, with that device current: look the array's device
+// address up (no allocation).  Runs inside the first mla_decode_noalloc call on
+// the device.
+int32_t noalloc_scratch(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_mla_noalloc_scratch) != cudaSuccess || a == nullptr) return MLA_ERR_CUDA;
+    g_noalloc_ptr[dev] = a;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" int32_t mla_decode_noalloc(const mla_decode_params* p, const void* q_nope_absorbed, const void* q_rope,
+                                      const void* kv_pages, const int32_t* block_table,
+                                      const int32_t* cache_seqlens, float scale, void* out, float* lse,
+                                      void* stream) {
+  int32_t st = check_params(p);
+  if (st != MLA_OK) return st;
+  size_t sched_bytes = 0, workspace_bytes = 0;
+  if ((st = mla_get_workspace_size(p, &sched_bytes, &workspace_bytes)) != MLA_OK) return st;
+  const size_t sched_region = align256(sched_bytes);
+  if (sched_region + workspace_bytes > (size_t)MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != MLA_OK) return st;
+  // The scheduler kernel rewrites all of the metadata, and every split partial is
+  // written by the decode kernel before the combine reads it, so nothing in the
+  // array has to start at zero.
+  void* sched = scratch;
+  void* workspace = static_cast<char*>(scratch) + sched_region;
+  if ((st = mla_get_scheduler_metadata(p, cache_seqlens, sched, stream)) != MLA_OK) return st;
+  return mla_decode(p, q_nope_absorbed, q_rope, kv_pages, block_table, cache_seqlens, scale, out, lse, sched,
+                    workspace, stream);
+}
