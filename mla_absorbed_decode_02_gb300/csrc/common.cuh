@@ -18,7 +18,7 @@ __device__ int g_mla_error = 0;
 
 enum WaitSite : int {
   kSiteQEmpty = 1, kSiteKvEmpty, kSiteQFull, kSiteKvFull, kSiteSEmpty, kSitePFull, kSiteSFull,
-  kSiteXFree, kSiteXFull, kSitePEmpty, kSiteDrain, kSiteSelftest,
+  kSiteXFree, kSiteXFull, kSitePEmpty, kSiteDrain, kSiteSelftest, kSiteML,
 };
 
 struct WaitCtx {
@@ -33,12 +33,12 @@ __device__ __forceinline__ void raise_abort(const WaitCtx& w, int site) {
   if (w.abort_peer) asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(w.abort_peer), "r"(1) : "memory");
 }
 
-// Bounded wait by one thread.  Returns false if the CTA is aborting or the wait
-// ran out (then it raises the abort for this CTA and its peer).
+// Bounded wait by one thread (the slow path, out of line).  Returns false if
+// the CTA is aborting or the wait ran out (then it raises the abort for this
+// CTA and its peer).
 template <bool kClusterScope = false>
-__device__ __noinline__ bool wait_one(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
   auto poll = [&]() { return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-  if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (poll()) return true;
@@ -52,10 +52,17 @@ __device__ __noinline__ bool wait_one(uint32_t bar, uint32_t parity, const WaitC
   }
 }
 
+// Bounded wait by one thread: one inline poll, then the slow path.
+template <bool kClusterScope = false>
+__device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
+  if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  return wait_slow<kClusterScope>(bar, parity, w, site);
+}
+
 // Bounded wait by a whole warp; the result is the same in every lane.
 template <bool kClusterScope = false>
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
-  bool ok = wait_one<kClusterScope>(bar, parity, w, site);
+  const bool ok = wait_one<kClusterScope>(bar, parity, w, site);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -15,26 +15,32 @@
 // (st.async), encoded as 16-bit block floating point -- one shared exponent per
 // (head, 32-token chunk), 16-bit signed mantissas.  Each CTA adds the peer's
 // rounded half to its own exact half, runs the online softmax for its output
-// half (one thread per head row and 32-token chunk), writes P (bf16) to shared
-// memory, and accumulates O_half += P V_half (tcgen05.mma, N = 256, V read
-// MN-major from the same shared-memory page the score used).
+// half, writes P (bf16) to shared memory, and accumulates O_half += P V_half
+// (tcgen05.mma, N = 256, V read MN-major from the same shared-memory page the
+// score used).
 //
 // "MLA inference: two computation paths and FlashMLA", section "Decode
 // attention becomes a compute problem": the 128 heads are the M dimension of
 // the matrix multiply, a block of KV is staged in shared memory, long
 // sequences are split across SMs and merged through their LSE.
 //
+// Softmax warpgroups.  Two warpgroups take the tiles in turn (warpgroup w owns
+// the tiles of parity w, thread = head row = TMEM lane, all 64 columns of the
+// row), so the two run their exchange waits and exponentials overlapped, each
+// with its own score buffer, exchange slot and P buffer.  The only per-tile
+// link between them is the running row maximum (the max of tile t is decided
+// from the one of tile t-1, through shared memory); each keeps its own part of
+// the row sum and the epilogue adds the two.  The maximum is raised lazily
+// (only when a tile's max exceeds it by more than 8 in log2 units), and O is
+// rescaled only then.
+//
 // Pipelining.  Four 36 KB shared-memory stages (a page stays resident from its
 // load through QK, softmax and PV, because the latent is key and value at
-// once); two score buffers in tensor memory; two exchange slots per chunk.  The
-// MMA warp issues QK ahead of PV.  The softmax warps run one tile ahead on the
-// exchange: while they receive tile i and turn it into P, they already encode
-// and send tile i+1.
+// once); the MMA warp issues QK(t) before PV(t-1).
 //
 // Warp roles (384 threads): warp 0 = TMA producer, warp 1 = MMA issuer,
-// warp 2 = tensor-memory allocator, warp 3 idle, warps 4..11 = softmax /
-// exchange / epilogue in two warpgroups, one per 32-token half of a tile
-// (thread = head row = TMEM lane).
+// warp 2 = tensor-memory allocator, warp 3 idle, warps 4..7 / 8..11 = softmax
+// warpgroups 0 / 1.
 #pragma once
 #include "common.cuh"
 
@@ -44,45 +50,46 @@ constexpr int kThreads = 384;
 constexpr int kRows = 128;      // MMA M: head rows (H <= 128, padded with zero queries)
 constexpr int kTileTok = 64;    // tokens per work tile (one page)
 constexpr int kStages = 4;
-constexpr int kChunks = 2;      // 32-token exchange chunks per tile
 
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t kLatBlock = 8192;                  // [64 rows x 128 B]: 64 latent dims of a page
 constexpr uint32_t kStageRope = 4 * kLatBlock;        // RoPE half [64 rows x 64 B]
 constexpr uint32_t kStageBytes = kStageRope + 4096;   // 36 KB
-constexpr uint32_t SM_P = kStages * kStageBytes;      // P: [128 rows x 128 B] bf16, 128-byte swizzle
-constexpr uint32_t SM_QR = SM_P + 16384;              // RoPE-query half [128 x 64 B], 64-byte swizzle
-constexpr uint32_t SM_X = SM_QR + 8192;               // peer partial scores: [slot][chunk][4][128 rows][16 B]
-constexpr uint32_t SM_XE = SM_X + 2 * kChunks * 8192; // peer exponents: [slot][chunk][128 rows] int32
-constexpr uint32_t SM_MX = SM_XE + 2 * kChunks * 512; // chunk maxima [2][2][128] f32 + row sums [2][128] f32
-constexpr uint32_t SM_BAR = SM_MX + 4096;
+constexpr uint32_t kPBytes = kRows * 128;             // one P buffer: [128 rows x 128 B] bf16, 128-byte swizzle
+constexpr uint32_t SM_P = kStages * kStageBytes;      // P[tile parity]
+constexpr uint32_t SM_QR = SM_P + 2 * kPBytes;        // RoPE-query half [128 x 64 B], 64-byte swizzle
+constexpr uint32_t kXSlot = 8 * kRows * 16;           // peer partial scores of one tile: [8][128 rows][16 B]
+constexpr uint32_t SM_X = SM_QR + 8192;               // exchange slots [tile parity]
+constexpr uint32_t SM_XE = SM_X + 2 * kXSlot;         // peer exponent pairs [tile parity][128 rows] u32
+constexpr uint32_t SM_ML = SM_XE + 2 * kRows * 4;     // published running max / row sum: [parity][2][128] f32
+constexpr uint32_t SM_BAR = SM_ML + 2 * 2 * kRows * 4;
 constexpr uint32_t kSmemBytes = SM_BAR + 512 + 1024;  // + alignment slack
-constexpr uint32_t kXChunkBytes = kRows * (64 + 4);   // bytes one CTA sends the other per chunk
+constexpr uint32_t kXBytes = kRows * (128 + 4);       // bytes one CTA sends the other per tile
 
 // tensor memory columns
 constexpr uint32_t TM_O = 0, TM_S = 256, TM_Q = 384;  // S buffers at 256 and 320
 
-// barrier slots (8 bytes each) inside SM_BAR
+// barrier slots (8 bytes each) inside SM_BAR; "[parity]" = + tile parity
 enum : uint32_t {
   B_QR_FULL = 0,
   B_QR_EMPTY,
   B_QT_FULL,
-  B_P_FULL,
-  B_PV_DONE,
   B_DRAIN,
-  B_MX,
-  B_EPI,
   B_KV_FULL,                        // + stage
   B_KV_EMPTY = B_KV_FULL + kStages,
-  B_S_FULL = B_KV_EMPTY + kStages,  // + buffer
-  B_S_EMPTY = B_S_FULL + 2,
-  B_X_FULL = B_S_EMPTY + 2,         // + 2 * slot + chunk
-  B_X_FREE = B_X_FULL + 2 * kChunks,
-  kNumBars = B_X_FREE + 2 * kChunks
+  B_S_FULL = B_KV_EMPTY + kStages,  // [parity] QK(t) done
+  B_S_EMPTY = B_S_FULL + 2,         // [parity] scores of tile t read out
+  B_P_FULL = B_S_EMPTY + 2,         // [parity] P(t) written
+  B_P_FREE = B_P_FULL + 2,          // [parity] PV(t) done
+  B_X_FULL = B_P_FREE + 2,          // [parity] the peer's partial scores of tile t arrived
+  B_X_FREE = B_X_FULL + 2,          // [parity] the peer consumed what this CTA sent for tile t
+  B_ML = B_X_FREE + 2,              // [parity] running max / row sum of tile t published
+  kNumBars = B_ML + 2
 };
 constexpr uint32_t OFF_TMEM_SLOT = kNumBars * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
 static_assert(OFF_ABORT + 4 <= 512, "barrier area");
+static_assert(kSmemBytes <= 232448, "shared memory");
 
 struct Piece {
   int qb, t0, t1, split;
@@ -223,24 +230,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(bar(B_QR_FULL), 1);
     mbar_init(bar(B_QR_EMPTY), 1);
-    // softmax-side barriers count one arrival per softmax warp (8), after __syncwarp
-    mbar_init(bar(B_QT_FULL), 8);
-    mbar_init(bar(B_P_FULL), 8);
-    mbar_init(bar(B_MX), 8);
-    mbar_init(bar(B_EPI), 8);
-    mbar_init(bar(B_PV_DONE), 1);
+    mbar_init(bar(B_QT_FULL), 4);  // the four warps of the warpgroup that loads the query half
     mbar_init(bar(B_DRAIN), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(B_KV_FULL + s), 1);
       mbar_init(bar(B_KV_EMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_S_FULL + s), 1);
-      mbar_init(bar(B_S_EMPTY + s), 8);
-    }
-    for (int c = 0; c < 2 * kChunks; ++c) {
-      mbar_init(bar(B_X_FULL + c), 1);
-      mbar_init(bar(B_X_FREE + c), 4);  // one arrival per peer softmax warp of that chunk
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(bar(B_S_FULL + p), 1);   // MMA commit
+      mbar_init(bar(B_S_EMPTY + p), 4);  // one arrival per warp of warpgroup p
+      mbar_init(bar(B_P_FULL + p), 4);
+      mbar_init(bar(B_P_FREE + p), 1);   // MMA commit
+      mbar_init(bar(B_X_FULL + p), 1);   // receiver's expect_tx arrival + the peer's st.async bytes
+      mbar_init(bar(B_X_FREE + p), 4);   // one remote arrival per warp of the peer's warpgroup p
+      mbar_init(bar(B_ML + p), 4);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -305,8 +308,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    // Order: QK(t), then PV(t-2): the scores run ahead of the PV products, so the
-    // softmax warps find the next tile's scores ready when they need them.
+    // Order: QK(t), then PV(t-1).  A score buffer is read out right after its QK,
+    // so QK(t) rarely waits, and PV(t-1) queues behind it.
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16_f32(128, 64, 0, 0);
       constexpr uint32_t id_pv = idesc_bf16_f32(128, 256, 0, 1);
@@ -317,19 +320,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool pv_first[4] = {false, false, false, false};  // first-of-piece flag of tile t, indexed t % 4
       bool ok = true;
       auto issue_pv = [&]() -> bool {
-        if (!wait_one(bar(B_P_FULL), pv_t & 1, wc, kSitePFull)) return false;
+        const uint32_t pb = pv_t & 1;
+        if (!wait_one(bar(B_P_FULL + pb), (pv_t >> 1) & 1, wc, kSitePFull)) return false;
         tc_fence_after();
         const uint32_t st = pv_t % kStages;
         const uint32_t sbase = base + st * kStageBytes;
         const bool acc = !pv_first[pv_t & 3];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint64_t a = smem_desc(base + SM_P + k * 32, 16, 1024, kSwizzle128B);
+          const uint64_t a = smem_desc(base + SM_P + pb * kPBytes + k * 32, 16, 1024, kSwizzle128B);
           const uint64_t bv = smem_desc(sbase + k * 2048, kLatBlock, 1024, kSwizzle128B);
           mma_bf16_ss(tmem + TM_O, a, bv, id_pv, (acc || k > 0) ? 1u : 0u);
         }
         mma_commit(bar(B_KV_EMPTY + st));
-        mma_commit(bar(B_PV_DONE));
+        mma_commit(bar(B_P_FREE + pb));
         ++pv_t;
         return true;
       };
@@ -358,7 +362,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (ti.last) mma_commit(bar(B_QR_EMPTY));
         pv_first[t & 3] = ti.first;
         ++t;
-        if (t >= 3 && !(ok = issue_pv())) break;  // PV(t-3) once QK(t-1) is queued
+        if (t >= 2 && !(ok = issue_pv())) break;  // PV(t-2) once QK(t-1) is queued
       }
       while (ok && pv_t < t) ok = issue_pv();
       // no MMA may still run when tensor memory is released
@@ -371,30 +375,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       wait_one(bar(B_DRAIN), 0, wd, kSiteDrain);
     }
   } else if (warp >= 4) {
-    // ================================================================ softmax / exchange / epilogue
-    // Two warpgroups; warpgroup cw handles score columns [32 cw, 32 cw + 32) of every
-    // tile (one exchange chunk), O columns [128 cw, 128 cw + 128) for rescale and
-    // epilogue, and query columns [64 cw, 64 cw + 64) of tensor memory.
-    const int cw = (warp - 4) >> 2;                   // column group
-    const int r = ((warp & 3) << 5) | lane;           // head row == TMEM lane
-    const int gt = tid - 128;                         // 0..255 across both groups
+    // ================================================================ softmax warpgroups
+    const uint32_t w = (uint32_t)(warp - 4) >> 2;  // this warpgroup owns the tiles of parity w
+    const int r = ((warp & 3) << 5) | lane;        // head row == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    // exchange slot (tile parity) x chunk: data at SM_X + (2 slot + cw) 8 KB, exponents at SM_XE + (2 slot + cw) 512 B
-    const uint32_t peer_x = map_to_rank(base + SM_X + cw * 8192, peer);
-    const uint32_t peer_xe = map_to_rank(base + SM_XE + cw * 512, peer);
     const uint32_t peer_bar0 = map_to_rank(bar(0), peer);  // the peer's barrier i is at peer_bar0 + 8 i
-    const uint32_t my_x = base + SM_X + cw * 8192, my_xe = base + SM_XE + cw * 512;
+    const uint32_t peer_x = map_to_rank(base + SM_X + w * kXSlot, peer);
+    const uint32_t peer_xe = map_to_rank(base + SM_XE + w * kRows * 4, peer);
+    const uint32_t my_x = base + SM_X + w * kXSlot, my_xe = base + SM_XE + w * kRows * 4;
+    float* ml = reinterpret_cast<float*>(smem + SM_ML);  // [parity][0 = max, 1 = row sum][128]
     const float sl2 = args.scale_log2;
     const int H = args.H;
     bool ok = true;
 
-    // absorbed-query columns of this group -> tensor memory (A operand of the latent score)
+    // absorbed-query half of query block qb -> tensor memory (A operand of the latent score)
     auto load_q_tmem = [&](int qb) {
-      uint32_t q[32];
-      const uint32_t* src =
-          reinterpret_cast<const uint32_t*>(args.q_nope) + ((int64_t)qb * H + r) * 256 + 128 * half + 64 * cw;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(args.q_nope) + ((int64_t)qb * H + r) * 256 + 128 * half;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t q[32];
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
           uint4 v = make_uint4(0, 0, 0, 0);
@@ -404,7 +403,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           q[j + 2] = v.z;
           q[j + 3] = v.w;
         }
-        tmem_st32(tmem + lane_off + TM_Q + 64 * cw + 32 * c, q);
+        tmem_st32(tmem + lane_off + TM_Q + 32 * c, q);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -412,274 +411,267 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_QT_FULL));
     };
 
-    PieceWalker qwalk = walker0;  // one piece ahead of the score loads: feeds the query loads
-    TileCursor cursor;
-    cursor.init(walker0);
-    uint32_t s_t = 0;     // tiles whose scores were read
-    uint32_t x_sent = 0;  // tiles sent to the peer
-    uint32_t x_recv = 0;  // tiles received from the peer (== tiles processed)
-    uint32_t pieces_done = 0;
-    float own_c[32], own_n[32];  // this CTA's exact partial scores (current / next tile)
-    uint32_t pk_n[16];           // next tile's partial scores in 16-bit block floating point
-    int ex_n = 0;
-
-    // A: this group's score columns of a tile -> registers + block-float encoding
-    auto stage_a = [&](const TileInfo& x, float (&own)[32]) -> bool {
-      const uint32_t sb = s_t & 1;
-      if (!wait_warp(bar(B_S_FULL + sb), (s_t >> 1) & 1, wc, kSiteSFull)) return false;
-      tc_fence_after();
-      uint32_t v[32];
-      tmem_ld32(tmem + lane_off + TM_S + 64 * sb + 32 * cw, v);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_S_EMPTY + sb));
-      ++s_t;
-      const int valid = x.valid - 32 * cw;
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-      if (valid >= 32) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          own[j] = __uint_as_float(v[j]);
-          own[j + 1] = __uint_as_float(v[j + 1]);
-          own[j + 2] = __uint_as_float(v[j + 2]);
-          own[j + 3] = __uint_as_float(v[j + 3]);
-          a0 = fmaxf(a0, fabsf(own[j]));
-          a1 = fmaxf(a1, fabsf(own[j + 1]));
-          a2 = fmaxf(a2, fabsf(own[j + 2]));
-          a3 = fmaxf(a3, fabsf(own[j + 3]));
-        }
-      } else {  // last tile of a sequence: columns past the end are sent as 0 and masked later
-#pragma unroll
-        for (int j = 0; j < 32; ++j) own[j] = (j < valid) ? __uint_as_float(v[j]) : 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          a0 = fmaxf(a0, fabsf(own[j]));
-          a1 = fmaxf(a1, fabsf(own[j + 1]));
-          a2 = fmaxf(a2, fabsf(own[j + 2]));
-          a3 = fmaxf(a3, fabsf(own[j + 3]));
-        }
-      }
-      const int e = bfp_exponent(fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)));
-      ex_n = e;
-      const float k = pow2f(15 - e);
-#pragma unroll
-      for (int u = 0; u < 16; ++u) pk_n[u] = bfp_pack2(own[2 * u] * k, own[2 * u + 1] * k);
-      if (x.last) {  // the query half in tensor memory is free once the last score of its piece exists
-        Piece np;
-        if (qwalk.next(np)) load_q_tmem(np.qb);
-      }
-      return true;
-    };
-    // slot = tile parity, so a send only waits for the peer to have consumed the tile before last
-    auto send_chunk = [&]() -> bool {
-      const uint32_t slot = x_sent & 1;
-      if (!wait_warp(bar(B_X_FREE + 2 * slot + cw), ((x_sent >> 1) & 1) ^ 1, wc, kSiteXFree)) return false;
-      const uint32_t full = peer_bar0 + 8 * (B_X_FULL + 2 * slot + cw);
-      const uint32_t dst = peer_x + slot * 2 * 8192, dste = peer_xe + slot * 2 * 512;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        st_async_v4(dst + (j * 128 + r) * 16, pk_n[4 * j], pk_n[4 * j + 1], pk_n[4 * j + 2], pk_n[4 * j + 3], full);
-      st_async_b32(dste + r * 4, (uint32_t)ex_n, full);
-      ++x_sent;
-      return true;
-    };
-
-    // epilogue of a finished piece (run one tile later, when its last PV is long done)
+    // epilogue of a finished piece: O / l -> out (or a split partial), lse
+    int epi_qb = 0, epi_split = 0, epi_piece = -1;
     bool epi_pending = false;
-    int epi_qb = 0, epi_split = 0;
-    float epi_m = 0.f, epi_l = 1.f;
-    auto epilogue = [&]() -> bool {
-      // total row sum = both groups' partial sums
-      float* lx = reinterpret_cast<float*>(smem + SM_MX) + 2 * 128 * 2;  // [group][row] after the max buffers
-      lx[cw * 128 + r] = epi_l;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_EPI));
-      if (!wait_warp(bar(B_EPI), pieces_done & 1, wc, kSitePEmpty)) return false;
-      const float ltot = lx[r] + lx[128 + r];
-      ++pieces_done;
+    auto epilogue = [&](float m_fin, float l_tot) {
       const bool split = num_splits[epi_qb] > 1;
       const int slot = split ? split_offset[epi_qb] + epi_split : 0;
-      const float inv_l = 1.f / ltot;
+      const float inv_l = 1.f / l_tot;
       const bool write_row = r < H;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + TM_O + 128 * cw + 32 * c, v);
+      for (int c = 0; c < 8; c += 2) {
+        uint32_t v[2][32];
+        tmem_ld32(tmem + lane_off + TM_O + 32 * c, v[0]);
+        tmem_ld32(tmem + lane_off + TM_O + 32 * c + 32, v[1]);
         tmem_wait_ld();
         if (write_row) {
-          const int d0 = 256 * half + 128 * cw + 32 * c;
-          if (split || args.out_f32) {
-            float* dst = split ? args.o_acc + ((int64_t)slot * H + r) * 512 + d0
-                               : reinterpret_cast<float*>(args.out) + ((int64_t)epi_qb * H + r) * 512 + d0;
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4*>(dst + j) =
-                  make_float4(__uint_as_float(v[j]) * inv_l, __uint_as_float(v[j + 1]) * inv_l,
-                              __uint_as_float(v[j + 2]) * inv_l, __uint_as_float(v[j + 3]) * inv_l);
-          } else {
-            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.out) + ((int64_t)epi_qb * H + r) * 512 + d0;
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int d0 = 256 * half + 32 * (c + h2);
+            if (split || args.out_f32) {
+              float* dst = split ? args.o_acc + ((int64_t)slot * H + r) * 512 + d0
+                                 : reinterpret_cast<float*>(args.out) + ((int64_t)epi_qb * H + r) * 512 + d0;
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              uint4 o;
-              o.x = pack_bf16(__uint_as_float(v[j]) * inv_l, __uint_as_float(v[j + 1]) * inv_l);
-              o.y = pack_bf16(__uint_as_float(v[j + 2]) * inv_l, __uint_as_float(v[j + 3]) * inv_l);
-              o.z = pack_bf16(__uint_as_float(v[j + 4]) * inv_l, __uint_as_float(v[j + 5]) * inv_l);
-              o.w = pack_bf16(__uint_as_float(v[j + 6]) * inv_l, __uint_as_float(v[j + 7]) * inv_l);
-              *reinterpret_cast<uint4*>(dst + j) = o;
+              for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(dst + j) =
+                    make_float4(__uint_as_float(v[h2][j]) * inv_l, __uint_as_float(v[h2][j + 1]) * inv_l,
+                                __uint_as_float(v[h2][j + 2]) * inv_l, __uint_as_float(v[h2][j + 3]) * inv_l);
+            } else {
+              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.out) + ((int64_t)epi_qb * H + r) * 512 + d0;
+#pragma unroll
+              for (int j = 0; j < 32; j += 8) {
+                uint4 o;
+                o.x = pack_bf16(__uint_as_float(v[h2][j]) * inv_l, __uint_as_float(v[h2][j + 1]) * inv_l);
+                o.y = pack_bf16(__uint_as_float(v[h2][j + 2]) * inv_l, __uint_as_float(v[h2][j + 3]) * inv_l);
+                o.z = pack_bf16(__uint_as_float(v[h2][j + 4]) * inv_l, __uint_as_float(v[h2][j + 5]) * inv_l);
+                o.w = pack_bf16(__uint_as_float(v[h2][j + 6]) * inv_l, __uint_as_float(v[h2][j + 7]) * inv_l);
+                *reinterpret_cast<uint4*>(dst + j) = o;
+              }
             }
           }
         }
       }
-      if (write_row && half == 0 && cw == 0) {
-        const float lse = (epi_m + log2f(ltot)) * 0.69314718055994530942f;
+      if (write_row && half == 0) {
+        const float lse = (m_fin + log2f(l_tot)) * 0.69314718055994530942f;
         if (split)
           args.lse_acc[(int64_t)slot * H + r] = lse;
         else
           args.lse[(int64_t)epi_qb * H + r] = lse;
       }
       tc_fence_before();
-      epi_pending = false;
-      return true;
     };
 
-    TileInfo cur, nxt;
-    bool have = cursor.next(cur);
-    if (have) {
-      Piece p0;
-      qwalk.next(p0);
-      load_q_tmem(p0.qb);
-      ok = stage_a(cur, own_c) && send_chunk();
-    }
-    float m_used = -INFINITY, l = 0.f;  // running max (log2 units) and this group's row sum
-    uint32_t kv_t = 0;
-    float* mx = reinterpret_cast<float*>(smem + SM_MX);  // [tile parity][group][row] chunk maxima
-    while (ok && have) {
-      const bool have_n = cursor.next(nxt);
-      if (have_n && !(ok = stage_a(nxt, own_n))) break;
-      if (cur.first) {
-        m_used = -INFINITY;
-        l = 0.f;
+    PieceWalker ahead = walker0;  // one piece ahead of the tile walk: feeds the query loads
+    Piece np;
+    bool has_np = ahead.next(np);  // piece 0
+    if (w == 0 && has_np) load_q_tmem(np.qb);
+
+    float l_mine = 0.f, m_ref = 0.f;  // this warpgroup's part of the row sum, relative to m_ref
+    int my_piece = -1;                // piece that l_mine belongs to
+    TileCursor cursor;
+    cursor.init(walker0);
+    TileInfo x;
+    uint32_t t = 0;
+    int piece = -1;
+    while (ok && cursor.next(x)) {
+      if (x.first) {
+        ++piece;
+        has_np = ahead.next(np);  // the piece after this one
       }
-      // ---- B: the next tile's chunk goes out; receive the peer's half of this tile's chunk
-      if (have_n && !(ok = send_chunk())) break;
-      const uint32_t rslot = x_recv & 1;
-      if (lane == 0 && (warp & 3) == 0) mbar_arrive_expect_tx(bar(B_X_FULL + 2 * rslot + cw), kXChunkBytes);
-      if (!(ok = wait_warp<true>(bar(B_X_FULL + 2 * rslot + cw), (x_recv >> 1) & 1, wc, kSiteXFull))) break;
-      uint32_t wv[16];
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(wv[4 * j]), "=r"(wv[4 * j + 1]), "=r"(wv[4 * j + 2]), "=r"(wv[4 * j + 3])
-                     : "r"(my_x + rslot * 2 * 8192 + (j * 128 + r) * 16));
-      int pe;
-      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pe) : "r"(my_xe + rslot * 2 * 512 + r * 4));
-      const float kp = pow2f(pe - 15);
-      const int vc = cur.valid - 32 * cw;
-      float sc[32];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        float q0, q1;
-        bfp_unpack2(wv[u], q0, q1);
-        sc[2 * u] = fmaf(q0, kp, own_c[2 * u]) * sl2;
-        sc[2 * u + 1] = fmaf(q1, kp, own_c[2 * u + 1]) * sl2;
-      }
-      __syncwarp();  // every lane has consumed its part of the slot
-      if (lane == 0) mbar_arrive_remote(peer_bar0 + 8 * (B_X_FREE + 2 * rslot + cw));
-      if (vc < 32) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sc[j] = (j < vc) ? sc[j] : -INFINITY;
-      }
-      float c0 = sc[0], c1 = sc[1], c2 = sc[2], c3 = sc[3];
-#pragma unroll
-      for (int j = 4; j < 32; j += 4) {
-        c0 = fmaxf(c0, sc[j]);
-        c1 = fmaxf(c1, sc[j + 1]);
-        c2 = fmaxf(c2, sc[j + 2]);
-        c3 = fmaxf(c3, sc[j + 3]);
-      }
-      // ---- tile max across the two groups (shared memory, one barrier per tile)
-      const uint32_t par = x_recv & 1;
-      mx[(par * 2 + cw) * 128 + r] = fmaxf(fmaxf(c0, c1), fmaxf(c2, c3));
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_MX));
-      if (!(ok = wait_warp(bar(B_MX), par, wc, kSiteSFull))) break;
-      const float cm = fmaxf(mx[(par * 2) * 128 + r], mx[(par * 2 + 1) * 128 + r]);
-      float o_alpha = 1.f;
-      if (cur.first) {
-        m_used = cm;  // finite: token 0 of a piece's first tile is visible
-      } else if (cm > m_used + 8.f) {  // lazy rescale: only when the max grows a lot
-        o_alpha = exp2f(m_used - cm);
-        m_used = cm;
-        l *= o_alpha;
-      }
-      uint32_t pp[16];
-      float r0 = 0.f, r1 = 0.f;
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const float p0 = exp2f(sc[2 * u] - m_used), p1 = exp2f(sc[2 * u + 1] - m_used);
-        pp[u] = pack_bf16(p0, p1);
-        r0 += p0;
-        r1 += p1;
-      }
-      l += r0 + r1;
-      ++x_recv;
-      // ---- C: the previous PV is done -> finish the previous piece, fix O, publish P
-      if (kv_t > 0 && !(ok = wait_warp(bar(B_PV_DONE), (kv_t - 1) & 1, wc, kSitePEmpty))) break;
-      tc_fence_after();
-      if (epi_pending && !(ok = epilogue())) break;
-      if (!cur.first && __any_sync(0xffffffffu, o_alpha != 1.f)) {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + TM_O + 128 * cw + 32 * c, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * o_alpha);
-          tmem_st32(tmem + lane_off + TM_O + 128 * cw + 32 * c, v);
-        }
-        tmem_wait_st();
-      }
-      const uint32_t st = kv_t % kStages;
-      if (cur.valid < kTileTok) {
-        // rows past the sequence end must not reach the PV product (0 * garbage): zero them
-        if (!(ok = wait_warp(bar(B_KV_FULL + st), (kv_t / kStages) & 1, wc, kSiteKvFull))) break;
-        const uint32_t sbase = base + st * kStageBytes;
-        const int nz = (kTileTok - cur.valid) * 4 * 8;  // 16-byte chunks: rows x 4 blocks x 8
-        for (int idx = gt; idx < nz; idx += 256) {
-          const int row = cur.valid + idx / 32, blk = (idx / 8) & 3, ch = idx & 7;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(sbase + blk * kLatBlock + row * 128 + ch * 16),
-                       "r"(0u));
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {  // this group's 32 P values of the row (K-major, 128-byte swizzle)
-        const uint32_t ch = 4 * cw + q;
-        const uint32_t a = base + SM_P + r * 128 + ((ch ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(pp[4 * q]), "r"(pp[4 * q + 1]),
-                     "r"(pp[4 * q + 2]), "r"(pp[4 * q + 3]));
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_P_FULL));
-      ++kv_t;
-      if (cur.last) {
-        epi_pending = true;
-        epi_qb = cur.qb;
-        epi_split = cur.split;
-        epi_m = m_used;
-        epi_l = l;
-      }
-      if (!have_n) break;
-      cur = nxt;
-#pragma unroll
-      for (int u = 0; u < 32; ++u) own_c[u] = own_n[u];
-    }
-    if (ok && epi_pending) {
-      if (wait_warp(bar(B_PV_DONE), (kv_t - 1) & 1, wc, kSitePEmpty)) {
+      if ((t & 1) == w) {
+        const uint32_t sb = w, ph = (t >> 1) & 1;
+        // ---- own partial scores; the score buffer is free again right after the read
+        if (!(ok = wait_warp(bar(B_S_FULL + sb), ph, wc, kSiteSFull))) break;
         tc_fence_after();
-        epilogue();
+        float sc[64];
+        {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tmem + lane_off + TM_S + 64 * sb, v0);
+          tmem_ld32(tmem + lane_off + TM_S + 64 * sb + 32, v1);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_S_EMPTY + sb));
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            sc[j] = __uint_as_float(v0[j]);
+            sc[32 + j] = __uint_as_float(v1[j]);
+          }
+        }
+        // the query half in tensor memory is free once the last score of its piece exists
+        if (x.last && has_np) load_q_tmem(np.qb);
+        const int valid = x.valid;
+        if (valid < kTileTok) {  // columns past the sequence end: sent as 0, masked below
+#pragma unroll
+          for (int j = 0; j < 64; ++j) sc[j] = (j < valid) ? sc[j] : 0.f;
+        }
+        // ---- encode (16-bit block floating point, one exponent per 32 columns) and send
+        {
+          float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            a0 = fmaxf(a0, fabsf(sc[j]));
+            a1 = fmaxf(a1, fabsf(sc[j + 1]));
+            b0 = fmaxf(b0, fabsf(sc[32 + j]));
+            b1 = fmaxf(b1, fabsf(sc[32 + j + 1]));
+          }
+          const int e0 = bfp_exponent(fmaxf(a0, a1)), e1 = bfp_exponent(fmaxf(b0, b1));
+          const float k0 = pow2f(15 - e0), k1 = pow2f(15 - e1);
+          uint32_t pk[32];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            pk[u] = bfp_pack2(sc[2 * u] * k0, sc[2 * u + 1] * k0);
+            pk[16 + u] = bfp_pack2(sc[32 + 2 * u] * k1, sc[32 + 2 * u + 1] * k1);
+          }
+          if (!(ok = wait_warp(bar(B_X_FREE + sb), ph ^ 1, wc, kSiteXFree))) break;
+          const uint32_t full = peer_bar0 + 8 * (B_X_FULL + sb);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_async_v4(peer_x + (j * kRows + r) * 16, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3], full);
+          st_async_b32(peer_xe + r * 4, ((uint32_t)e0 & 0xFFFFu) | ((uint32_t)e1 << 16), full);
+        }
+        // ---- the peer's half of the same scores
+        if ((warp & 3) == 0 && lane == 0) mbar_arrive_expect_tx(bar(B_X_FULL + sb), kXBytes);
+        if (!(ok = wait_warp<true>(bar(B_X_FULL + sb), ph, wc, kSiteXFull))) break;
+        {
+          uint32_t pe;
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pe) : "r"(my_xe + r * 4));
+          const float kp0 = pow2f((int)(int16_t)(pe & 0xFFFFu) - 15), kp1 = pow2f(((int)pe >> 16) - 15);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint32_t wv[4];
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(wv[0]), "=r"(wv[1]), "=r"(wv[2]), "=r"(wv[3])
+                         : "r"(my_x + (j * kRows + r) * 16));
+            const float kp = j < 4 ? kp0 : kp1;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              float q0, q1;
+              bfp_unpack2(wv[u], q0, q1);
+              sc[8 * j + 2 * u] = fmaf(q0, kp, sc[8 * j + 2 * u]) * sl2;
+              sc[8 * j + 2 * u + 1] = fmaf(q1, kp, sc[8 * j + 2 * u + 1]) * sl2;
+            }
+          }
+          __syncwarp();  // every lane has consumed its part of the slot
+          if (lane == 0) mbar_arrive_remote(peer_bar0 + 8 * (B_X_FREE + sb));
+        }
+        if (valid < kTileTok) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) sc[j] = (j < valid) ? sc[j] : -INFINITY;
+        }
+        float c0 = sc[0], c1 = sc[1], c2 = sc[2], c3 = sc[3];
+#pragma unroll
+        for (int j = 4; j < 64; j += 4) {
+          c0 = fmaxf(c0, sc[j]);
+          c1 = fmaxf(c1, sc[j + 1]);
+          c2 = fmaxf(c2, sc[j + 2]);
+          c3 = fmaxf(c3, sc[j + 3]);
+        }
+        const float cm = fmaxf(fmaxf(c0, c1), fmaxf(c2, c3));
+        // ---- running max: decided from the previous tile's (the other warpgroup's)
+        float m_prev = 0.f, l_other = 0.f;
+        if (t > 0) {
+          if (!(ok = wait_warp(bar(B_ML + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSiteML))) break;
+          m_prev = ml[((sb ^ 1) * 2) * kRows + r];
+          l_other = ml[((sb ^ 1) * 2 + 1) * kRows + r];
+        }
+        float m = m_prev, alpha = 1.f;
+        if (x.first) {
+          m = cm;  // finite: token 0 of a piece's first tile is visible
+        } else if (cm > m_prev + 8.f) {
+          m = cm;
+          alpha = exp2f(m_prev - cm);
+        }
+        // the finished piece (last tile t-1) takes both warpgroups' row sums at its final max
+        float epi_l = 0.f;
+        if (epi_pending) epi_l = l_other + (my_piece == epi_piece ? l_mine * exp2f(m_ref - m_prev) : 0.f);
+        uint32_t pp[32];
+        float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+#pragma unroll
+        for (int u = 0; u < 32; u += 2) {
+          const float p0 = exp2f(sc[2 * u] - m), p1 = exp2f(sc[2 * u + 1] - m);
+          const float p2 = exp2f(sc[2 * u + 2] - m), p3 = exp2f(sc[2 * u + 3] - m);
+          pp[u] = pack_bf16(p0, p1);
+          pp[u + 1] = pack_bf16(p2, p3);
+          r0 += p0;
+          r1 += p1;
+          r2 += p2;
+          r3 += p3;
+        }
+        if (piece != my_piece) {
+          my_piece = piece;
+          l_mine = 0.f;
+          m_ref = m;
+        }
+        l_mine = l_mine * exp2f(m_ref - m) + ((r0 + r1) + (r2 + r3));
+        m_ref = m;
+        ml[(sb * 2) * kRows + r] = m;
+        ml[(sb * 2 + 1) * kRows + r] = l_mine;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_ML + sb));
+        // ---- O is touched only after PV(t-1): the previous piece's epilogue, a rescale
+        const bool any_rescale = __any_sync(0xffffffffu, alpha != 1.f);
+        if (epi_pending || any_rescale) {
+          if (!(ok = wait_warp(bar(B_P_FREE + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSitePEmpty))) break;
+          tc_fence_after();
+          if (epi_pending) {
+            epilogue(m_prev, epi_l);
+            epi_pending = false;
+          }
+          if (any_rescale) {
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+              uint32_t v[32];
+              tmem_ld32(tmem + lane_off + TM_O + 32 * c, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+              tmem_st32(tmem + lane_off + TM_O + 32 * c, v);
+            }
+            tmem_wait_st();
+          }
+        }
+        // ---- publish P (its buffer is free once PV(t-2) is done)
+        if (!(ok = wait_warp(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) break;
+        if (valid < kTileTok) {
+          // rows past the sequence end must not reach the PV product (0 * garbage): zero them
+          const uint32_t sbase = base + (t % kStages) * kStageBytes;
+          const int nz = (kTileTok - valid) * 4 * 8;  // 16-byte chunks: rows x 4 blocks x 8
+          for (int idx = r; idx < nz; idx += kRows) {
+            const int row = valid + idx / 32, blk = (idx / 8) & 3, ch = idx & 7;
+            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(sbase + blk * kLatBlock + row * 128 + ch * 16),
+                         "r"(0u));
+          }
+        }
+        const uint32_t prow = base + SM_P + sb * kPBytes + r * 128;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)  // P row: K-major, 128-byte swizzle
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((((uint32_t)ch) ^ (r & 7)) << 4)),
+                       "r"(pp[4 * ch]), "r"(pp[4 * ch + 1]), "r"(pp[4 * ch + 2]), "r"(pp[4 * ch + 3]));
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_P_FULL + sb));
+      }
+      if (x.last) {  // the warpgroup of the next tile finishes this piece
+        epi_qb = x.qb;
+        epi_split = x.split;
+        epi_piece = piece;
+        epi_pending = ((t + 1) & 1) == w;
+      }
+      ++t;
+    }
+    if (ok && epi_pending) {  // the unit's last piece ended with the other warpgroup's tile t-1
+      const uint32_t pp = (t - 1) & 1;
+      if (wait_warp(bar(B_ML + pp), ((t - 1) >> 1) & 1, wc, kSiteML)) {
+        const float m_fin = ml[(pp * 2) * kRows + r];
+        const float l_other = ml[(pp * 2 + 1) * kRows + r];
+        const float l_tot = l_other + (my_piece == epi_piece ? l_mine * exp2f(m_ref - m_fin) : 0.f);
+        if (wait_warp(bar(B_P_FREE + pp), ((t - 1) >> 1) & 1, wc, kSitePEmpty)) {
+          tc_fence_after();
+          epilogue(m_fin, l_tot);
+        }
       }
     }
   }
