@@ -116,7 +116,7 @@ int32_t mla_get_scheduler_metadata(const mla_decode_params* p, const int32_t* ca
  *                    sequence b; entries past ceil(L_b/64) are never read.  Every entry read
  *                    must be in [0, num_pages).
  *   cache_seqlens    device int32 [B]; L_b includes the s_q new tokens; 0 <= L_b <= 64*max_pages
- *   scale            softmax scale (1/sqrt(192) for DeepSeek-V3 shapes)
+ *   scale            softmax scale, finite and > 0 (1/sqrt(192) for DeepSeek-V3 shapes)
  *   out              device [B][s_q][H][512], bf16 or float32 (out_dtype)
  *   lse              device float32 [B][s_q][H]; a token that sees no key gets out = 0, lse = -inf
  *   sched            device, from mla_get_scheduler_metadata with the same p and lengths

@@ -36,10 +36,11 @@
 //
 // Pipelining.  Four 36 KB shared-memory stages (a page stays resident from its
 // load through QK, softmax and PV, because the latent is key and value at
-// once); the MMA warp issues QK(t) before PV(t-1).
+// once).  QK and PV are issued by two different warps, so the scores of the
+// next tiles never wait for the P of the current one.
 //
-// Warp roles (384 threads): warp 0 = TMA producer, warp 1 = MMA issuer,
-// warp 2 = tensor-memory allocator, warp 3 idle, warps 4..7 / 8..11 = softmax
+// Warp roles (384 threads): warp 0 = TMA producer, warp 1 = QK issuer, warp 2
+// = tensor-memory allocator, warp 3 = PV issuer, warps 4..7 / 8..11 = softmax
 // warpgroups 0 / 1.
 #pragma once
 #include "common.cuh"
@@ -74,7 +75,8 @@ enum : uint32_t {
   B_QR_FULL = 0,
   B_QR_EMPTY,
   B_QT_FULL,
-  B_DRAIN,
+  B_DRAIN,                          // + issuer (0 = QK, 1 = PV)
+  B_DRAIN_PV,
   B_KV_FULL,                        // + stage
   B_KV_EMPTY = B_KV_FULL + kStages,
   B_S_FULL = B_KV_EMPTY + kStages,  // [parity] QK(t) done
@@ -168,6 +170,23 @@ __device__ __forceinline__ int bfp_exponent(float amax) {
   return e;
 }
 
+// Block floating point without conversion instructions.  Encode: x * 2^(14-e)
+// lies in (-2^14, 2^14); adding 1.5 * 2^23 in one FMA rounds it to an integer
+// (round to nearest even) held in the low mantissa bits, and the low 16 bits of
+// two such floats are packed into one word (two's-complement int16 each).
+// Decode: flip the sign bits (int16 -> offset binary u = v + 2^15), place u in
+// the mantissa of 2^23 (a float of value 2^23 + u) and subtract 2^23 + 2^15.
+// Both steps are exact.
+__device__ __forceinline__ uint32_t bfp_pack2_fast(float a, float b, float k) {
+  const uint32_t ia = __float_as_uint(fmaf(a, k, 12582912.0f)), ib = __float_as_uint(fmaf(b, k, 12582912.0f));
+  return __byte_perm(ia, ib, 0x5410);
+}
+__device__ __forceinline__ void bfp_unpack2_fast(uint32_t w, float& a, float& b) {
+  const uint32_t u = w ^ 0x80008000u;
+  a = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7410)) - 8421376.0f;
+  b = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7432)) - 8421376.0f;
+}
+
 // Two scaled scores -> two int16 mantissas (round to nearest even, saturating) in one word.
 __device__ __forceinline__ uint32_t bfp_pack2(float a, float b) {
   uint32_t w;
@@ -232,6 +251,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_QR_EMPTY), 1);
     mbar_init(bar(B_QT_FULL), 4);  // the four warps of the warpgroup that loads the query half
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_DRAIN_PV), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(B_KV_FULL + s), 1);
       mbar_init(bar(B_KV_EMPTY + s), 1);
@@ -306,73 +326,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ++t;
       }
     }
-  } else if (warp == 1) {
-    // ================================================================ MMA issuer
-    // Order: QK(t), then PV(t-1).  A score buffer is read out right after its QK,
-    // so QK(t) rarely waits, and PV(t-1) queues behind it.
+  } else if (warp == 1 || warp == 3) {
+    // ================================================================ MMA issuers
+    // warp 1: QK(t) as soon as the page is loaded and its score buffer was read out;
+    // warp 3: PV(t) as soon as P(t) is published.  The two touch disjoint tensor
+    // memory (scores / O) and only read shared memory.
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16_f32(128, 64, 0, 0);
       constexpr uint32_t id_pv = idesc_bf16_f32(128, 256, 0, 1);
       TileCursor cur;
       cur.init(walker0);
       TileInfo ti;
-      uint32_t t = 0, piece_no = 0, pv_t = 0;
-      bool pv_first[4] = {false, false, false, false};  // first-of-piece flag of tile t, indexed t % 4
-      bool ok = true;
-      auto issue_pv = [&]() -> bool {
-        const uint32_t pb = pv_t & 1;
-        if (!wait_one(bar(B_P_FULL + pb), (pv_t >> 1) & 1, wc, kSitePFull)) return false;
-        tc_fence_after();
-        const uint32_t st = pv_t % kStages;
-        const uint32_t sbase = base + st * kStageBytes;
-        const bool acc = !pv_first[pv_t & 3];
+      uint32_t t = 0, piece_no = 0;
+      if (warp == 1) {
+        while (cur.next(ti)) {
+          if (ti.first) {
+            if (!wait_one(bar(B_QR_FULL), piece_no & 1, wc, kSiteQFull)) break;
+            if (!wait_one(bar(B_QT_FULL), piece_no & 1, wc, kSiteQFull)) break;
+            ++piece_no;
+          }
+          const uint32_t st = t % kStages, sb = t & 1;
+          if (!wait_one(bar(B_KV_FULL + st), (t / kStages) & 1, wc, kSiteKvFull)) break;
+          if (!wait_one(bar(B_S_EMPTY + sb), ((t >> 1) & 1) ^ 1, wc, kSiteSEmpty)) break;
+          tc_fence_after();
+          const uint32_t sbase = base + st * kStageBytes;
+          const uint32_t d = tmem + TM_S + 64 * sb;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t a = smem_desc(base + SM_P + pb * kPBytes + k * 32, 16, 1024, kSwizzle128B);
-          const uint64_t bv = smem_desc(sbase + k * 2048, kLatBlock, 1024, kSwizzle128B);
-          mma_bf16_ss(tmem + TM_O, a, bv, id_pv, (acc || k > 0) ? 1u : 0u);
+          for (int k = 0; k < 16; ++k)  // latent half: A = query half in tensor memory
+            mma_bf16_ts(d, tmem + TM_Q + 8 * k,
+                        smem_desc(sbase + (k >> 2) * kLatBlock + (k & 3) * 32, 16, 1024, kSwizzle128B), id_qk,
+                        k > 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < 2; ++k)  // RoPE half: A = RoPE-query half in shared memory
+            mma_bf16_ss(d, smem_desc(base + SM_QR + 32 * k, 16, 512, kSwizzle64B),
+                        smem_desc(sbase + kStageRope + 32 * k, 16, 512, kSwizzle64B), id_qk, 1u);
+          mma_commit(bar(B_S_FULL + sb));
+          if (ti.last) mma_commit(bar(B_QR_EMPTY));
+          ++t;
         }
-        mma_commit(bar(B_KV_EMPTY + st));
-        mma_commit(bar(B_P_FREE + pb));
-        ++pv_t;
-        return true;
-      };
-      while (ok && cur.next(ti)) {
-        if (ti.first) {
-          if (!(ok = wait_one(bar(B_QR_FULL), piece_no & 1, wc, kSiteQFull))) break;
-          if (!(ok = wait_one(bar(B_QT_FULL), piece_no & 1, wc, kSiteQFull))) break;
-          ++piece_no;
+      } else {
+        while (cur.next(ti)) {
+          const uint32_t pb = t & 1, st = t % kStages;
+          if (!wait_one(bar(B_P_FULL + pb), (t >> 1) & 1, wc, kSitePFull)) break;
+          tc_fence_after();
+          const uint32_t sbase = base + st * kStageBytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t a = smem_desc(base + SM_P + pb * kPBytes + k * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bv = smem_desc(sbase + k * 2048, kLatBlock, 1024, kSwizzle128B);
+            mma_bf16_ss(tmem + TM_O, a, bv, id_pv, (!ti.first || k > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(B_KV_EMPTY + st));
+          mma_commit(bar(B_P_FREE + pb));
+          ++t;
         }
-        const uint32_t st = t % kStages, sb = t & 1;
-        if (!(ok = wait_one(bar(B_KV_FULL + st), (t / kStages) & 1, wc, kSiteKvFull))) break;
-        if (!(ok = wait_one(bar(B_S_EMPTY + sb), ((t >> 1) & 1) ^ 1, wc, kSiteSEmpty))) break;
-        tc_fence_after();
-        const uint32_t sbase = base + st * kStageBytes;
-        const uint32_t d = tmem + TM_S + 64 * sb;
-#pragma unroll
-        for (int k = 0; k < 16; ++k)  // latent half: A = query half in tensor memory
-          mma_bf16_ts(d, tmem + TM_Q + 8 * k,
-                      smem_desc(sbase + (k >> 2) * kLatBlock + (k & 3) * 32, 16, 1024, kSwizzle128B), id_qk,
-                      k > 0 ? 1u : 0u);
-#pragma unroll
-        for (int k = 0; k < 2; ++k)  // RoPE half: A = RoPE-query half in shared memory
-          mma_bf16_ss(d, smem_desc(base + SM_QR + 32 * k, 16, 512, kSwizzle64B),
-                      smem_desc(sbase + kStageRope + 32 * k, 16, 512, kSwizzle64B), id_qk, 1u);
-        mma_commit(bar(B_S_FULL + sb));
-        if (ti.last) mma_commit(bar(B_QR_EMPTY));
-        pv_first[t & 3] = ti.first;
-        ++t;
-        if (t >= 2 && !(ok = issue_pv())) break;  // PV(t-2) once QK(t-1) is queued
       }
-      while (ok && pv_t < t) ok = issue_pv();
-      // no MMA may still run when tensor memory is released
-      mma_commit(bar(B_DRAIN));
+      // no MMA of this issuer may still run when tensor memory is released
+      const uint32_t drain = bar(warp == 1 ? B_DRAIN : B_DRAIN_PV);
+      mma_commit(drain);
       WaitCtx wd = wc;
       wd.timeout_ns = 100000000ull;
       volatile int no_abort = 0;
       wd.abort_local = &no_abort;
       wd.abort_peer = 0;
-      wait_one(bar(B_DRAIN), 0, wd, kSiteDrain);
+      wait_one(drain, 0, wd, kSiteDrain);
     }
   } else if (warp >= 4) {
     // ================================================================ softmax warpgroups
@@ -499,6 +516,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             sc[32 + j] = __uint_as_float(v1[j]);
           }
         }
+        // this warpgroup's previous exchange slot was consumed long ago: hand it back
+        if (t >= 2 && lane == 0) mbar_arrive_remote(peer_bar0 + 8 * (B_X_FREE + sb));
         // the query half in tensor memory is free once the last score of its piece exists
         if (x.last && has_np) load_q_tmem(np.qb);
         const int valid = x.valid;
@@ -517,12 +536,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             b1 = fmaxf(b1, fabsf(sc[32 + j + 1]));
           }
           const int e0 = bfp_exponent(fmaxf(a0, a1)), e1 = bfp_exponent(fmaxf(b0, b1));
-          const float k0 = pow2f(15 - e0), k1 = pow2f(15 - e1);
+          const float k0 = pow2f(14 - e0), k1 = pow2f(14 - e1);
           uint32_t pk[32];
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
-            pk[u] = bfp_pack2(sc[2 * u] * k0, sc[2 * u + 1] * k0);
-            pk[16 + u] = bfp_pack2(sc[32 + 2 * u] * k1, sc[32 + 2 * u + 1] * k1);
+            pk[u] = bfp_pack2_fast(sc[2 * u], sc[2 * u + 1], k0);
+            pk[16 + u] = bfp_pack2_fast(sc[32 + 2 * u], sc[32 + 2 * u + 1], k1);
           }
           if (!(ok = wait_warp(bar(B_X_FREE + sb), ph ^ 1, wc, kSiteXFree))) break;
           const uint32_t full = peer_bar0 + 8 * (B_X_FULL + sb);
@@ -537,7 +556,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         {
           uint32_t pe;
           asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pe) : "r"(my_xe + r * 4));
-          const float kp0 = pow2f((int)(int16_t)(pe & 0xFFFFu) - 15), kp1 = pow2f(((int)pe >> 16) - 15);
+          const float kp0 = pow2f((int)(int16_t)(pe & 0xFFFFu) - 14), kp1 = pow2f(((int)pe >> 16) - 14);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             uint32_t wv[4];
@@ -548,13 +567,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               float q0, q1;
-              bfp_unpack2(wv[u], q0, q1);
-              sc[8 * j + 2 * u] = fmaf(q0, kp, sc[8 * j + 2 * u]) * sl2;
-              sc[8 * j + 2 * u + 1] = fmaf(q1, kp, sc[8 * j + 2 * u + 1]) * sl2;
+              bfp_unpack2_fast(wv[u], q0, q1);
+              sc[8 * j + 2 * u] = fmaf(q0, kp, sc[8 * j + 2 * u]);
+              sc[8 * j + 2 * u + 1] = fmaf(q1, kp, sc[8 * j + 2 * u + 1]);
             }
           }
-          __syncwarp();  // every lane has consumed its part of the slot
-          if (lane == 0) mbar_arrive_remote(peer_bar0 + 8 * (B_X_FREE + sb));
         }
         if (valid < kTileTok) {
 #pragma unroll
@@ -568,7 +585,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           c2 = fmaxf(c2, sc[j + 2]);
           c3 = fmaxf(c3, sc[j + 3]);
         }
-        const float cm = fmaxf(fmaxf(c0, c1), fmaxf(c2, c3));
+        const float cm = fmaxf(fmaxf(c0, c1), fmaxf(c2, c3)) * sl2;  // log2 units (sl2 > 0)
         // ---- running max: decided from the previous tile's (the other warpgroup's)
         float m_prev = 0.f, l_other = 0.f;
         if (t > 0) {
@@ -590,8 +607,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
 #pragma unroll
         for (int u = 0; u < 32; u += 2) {
-          const float p0 = exp2f(sc[2 * u] - m), p1 = exp2f(sc[2 * u + 1] - m);
-          const float p2 = exp2f(sc[2 * u + 2] - m), p3 = exp2f(sc[2 * u + 3] - m);
+          const float p0 = exp2f(fmaf(sc[2 * u], sl2, -m)), p1 = exp2f(fmaf(sc[2 * u + 1], sl2, -m));
+          const float p2 = exp2f(fmaf(sc[2 * u + 2], sl2, -m)), p3 = exp2f(fmaf(sc[2 * u + 3], sl2, -m));
           pp[u] = pack_bf16(p0, p1);
           pp[u + 1] = pack_bf16(p2, p3);
           r0 += p0;

@@ -263,7 +263,7 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
   const void* ptrs[] = {q_nope_absorbed, q_rope, kv_pages, block_table, cache_seqlens, out, lse, sched, workspace};
   for (const void* q : ptrs)
     if (!q || !aligned16(q)) return MLA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return MLA_ERR_INVALID_ARG;  // the kernel takes row maxima before scaling
   if (p->kv_dtype != MLA_KV_BF16) return MLA_ERR_UNSUPPORTED;
   DeviceInfo* dinfo = nullptr;
   if ((st = device_info(&dinfo)) != MLA_OK) return st;

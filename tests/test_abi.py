@@ -1,6 +1,7 @@
 """Host-side tests of the C ABI (no GPU needed): the library builds, loads and
 exports every entry point the header declares; argument checks; and the split
 planner (the same code the scheduler kernel runs) covers the work exactly once."""
+import ctypes
 import re
 
 import numpy as np
@@ -184,3 +185,12 @@ def test_plan_handles_empty_sequences(lib):
     pieces, ntiles, num_splits, _ = decode_plan(sched, 6, 1, True, seqlens)
     assert [num_splits[i] for i in (0, 2, 3, 5)] == [0, 0, 0, 0]
     assert sum(b - a for _, _, a, b, _ in pieces) == sum(ntiles) == -(-5 // TILE) + -(-300 // TILE)
+
+
+def test_non_positive_scale_is_rejected_before_any_launch(lib):
+    from mla_absorbed_decode_02_gb300 import MlaDecodeParams
+    p = MlaDecodeParams.make(batch=1, s_q=1, num_heads=128, num_pages=1, max_pages_per_seq=1, num_units=4)
+    buf = ctypes.c_void_p(256)  # never dereferenced: the scale check comes first
+    for scale in (0.0, -0.07, float("nan"), float("inf")):
+        st = lib.mla_decode_splitkv(ctypes.byref(p), buf, buf, buf, buf, buf, scale, buf, buf, buf, buf, None)
+        assert st == 1, scale
