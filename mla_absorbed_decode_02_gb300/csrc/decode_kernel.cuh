@@ -485,6 +485,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (w == 0 && has_np) load_q_tmem(np.qb);
 
     float l_mine = 0.f, m_ref = 0.f;  // this warpgroup's part of the row sum, relative to m_ref
+    uint32_t slot_dep = 0;            // computed from the last values read from the exchange slot
     int my_piece = -1;                // piece that l_mine belongs to
     TileCursor cursor;
     cursor.init(walker0);
@@ -516,8 +517,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             sc[32 + j] = __uint_as_float(v1[j]);
           }
         }
-        // this warpgroup's previous exchange slot was consumed long ago: hand it back
-        if (t >= 2 && lane == 0) mbar_arrive_remote(peer_bar0 + 8 * (B_X_FREE + sb));
+        // this warpgroup's previous exchange slot was consumed long ago: hand it back (a
+        // relaxed arrive, made to depend on the values read from the slot)
+        if (t >= 2 && lane == 0) mbar_arrive_remote_relaxed(peer_bar0 + 8 * (B_X_FREE + sb), slot_dep);
         // the query half in tensor memory is free once the last score of its piece exists
         if (x.last && has_np) load_q_tmem(np.qb);
         const int valid = x.valid;
@@ -556,6 +558,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         {
           uint32_t pe;
           asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pe) : "r"(my_xe + r * 4));
+          slot_dep = pe;
           const float kp0 = pow2f((int)(int16_t)(pe & 0xFFFFu) - 14), kp1 = pow2f(((int)pe >> 16) - 14);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -563,6 +566,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                          : "=r"(wv[0]), "=r"(wv[1]), "=r"(wv[2]), "=r"(wv[3])
                          : "r"(my_x + (j * kRows + r) * 16));
+            slot_dep ^= wv[0] ^ wv[3];
             const float kp = j < 4 ? kp0 : kp1;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {

@@ -51,6 +51,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
+// Relaxed arrive on a barrier of another CTA: no ordering with this thread's
+// earlier memory operations.  `dep` is an input the arrive waits for; pass a
+// value computed from earlier loads to make it follow their completion.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar, uint32_t dep) {
+  asm volatile("{\n\t.reg .b32 unused;\n\tmov.b32 unused, %1;\n\t"
+               "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];\n\t}" ::"r"(cluster_bar), "r"(dep)
+               : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
