@@ -158,8 +158,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Exponent e (clamped) with |x| < 2^e for the largest |x| of a chunk; the
 // 16-bit mantissa of x is then rint(x * 2^(15-e)).
@@ -170,6 +168,51 @@ __device__ __forceinline__ int bfp_exponent(float amax) {
   return e;
 }
 
+// Packed float pairs (the f32x2 arithmetic of sm_100-class GPUs: one instruction
+// for two lanes of a 64-bit register pair).
+__device__ __forceinline__ uint64_t pack_b32x2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  return pack_b32x2(__float_as_uint(lo), __float_as_uint(hi));
+}
+__device__ __forceinline__ uint64_t splat_f32x2(float v) { return pack_f32x2(v, v); }
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// 2^x on the special-function unit (inputs below -126 give 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Columns >= valid of a row of score pairs -> v.
+__device__ __forceinline__ void mask_pairs(uint64_t (&sc)[32], int valid, float v) {
+#pragma unroll
+  for (int u = 0; u < 32; ++u) {
+    float x0, x1;
+    unpack_f32x2(sc[u], x0, x1);
+    sc[u] = pack_f32x2(2 * u < valid ? x0 : v, 2 * u + 1 < valid ? x1 : v);
+  }
+}
+
 // Block floating point without conversion instructions.  Encode: x * 2^(14-e)
 // lies in (-2^14, 2^14); adding 1.5 * 2^23 in one FMA rounds it to an integer
 // (round to nearest even) held in the low mantissa bits, and the low 16 bits of
@@ -177,34 +220,15 @@ __device__ __forceinline__ int bfp_exponent(float amax) {
 // Decode: flip the sign bits (int16 -> offset binary u = v + 2^15), place u in
 // the mantissa of 2^23 (a float of value 2^23 + u) and subtract 2^23 + 2^15.
 // Both steps are exact.
-__device__ __forceinline__ uint32_t bfp_pack2_fast(float a, float b, float k) {
-  const uint32_t ia = __float_as_uint(fmaf(a, k, 12582912.0f)), ib = __float_as_uint(fmaf(b, k, 12582912.0f));
-  return __byte_perm(ia, ib, 0x5410);
+__device__ __forceinline__ uint32_t bfp_pack_pair(uint64_t xy, uint64_t k) {
+  float a, b;
+  unpack_f32x2(ffma_f32x2(xy, k, splat_f32x2(12582912.0f)), a, b);
+  return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x5410);
 }
-__device__ __forceinline__ void bfp_unpack2_fast(uint32_t w, float& a, float& b) {
+__device__ __forceinline__ uint64_t bfp_unpack_pair(uint32_t w) {
   const uint32_t u = w ^ 0x80008000u;
-  a = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7410)) - 8421376.0f;
-  b = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7432)) - 8421376.0f;
-}
-
-// Two scaled scores -> two int16 mantissas (round to nearest even, saturating) in one word.
-__device__ __forceinline__ uint32_t bfp_pack2(float a, float b) {
-  uint32_t w;
-  asm("{\n\t.reg .s16 lo, hi;\n\t"
-      "cvt.rni.sat.s16.f32 lo, %1;\n\t"
-      "cvt.rni.sat.s16.f32 hi, %2;\n\t"
-      "mov.b32 %0, {lo, hi};\n\t}"
-      : "=r"(w)
-      : "f"(a), "f"(b));
-  return w;
-}
-__device__ __forceinline__ void bfp_unpack2(uint32_t w, float& a, float& b) {
-  asm("{\n\t.reg .s16 lo, hi;\n\t"
-      "mov.b32 {lo, hi}, %2;\n\t"
-      "cvt.rn.f32.s16 %0, lo;\n\t"
-      "cvt.rn.f32.s16 %1, hi;\n\t}"
-      : "=f"(a), "=f"(b)
-      : "r"(w));
+  return fadd_f32x2(pack_b32x2(__byte_perm(u, 0x4B000000u, 0x7410), __byte_perm(u, 0x4B000000u, 0x7432)),
+                    splat_f32x2(-8421376.0f));
 }
 
 __device__ __forceinline__ void st_async_b32(uint32_t cluster_dst, uint32_t v, uint32_t cluster_bar) {
@@ -502,7 +526,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---- own partial scores; the score buffer is free again right after the read
         if (!(ok = wait_warp(bar(B_S_FULL + sb), ph, wc, kSiteSFull))) break;
         tc_fence_after();
-        float sc[64];
+        uint64_t sc[32];  // score pairs: columns (2u, 2u + 1) in pair u
         {
           uint32_t v0[32], v1[32];
           tmem_ld32(tmem + lane_off + TM_S + 64 * sb, v0);
@@ -512,9 +536,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_S_EMPTY + sb));
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            sc[j] = __uint_as_float(v0[j]);
-            sc[32 + j] = __uint_as_float(v1[j]);
+          for (int u = 0; u < 16; ++u) {
+            sc[u] = pack_b32x2(v0[2 * u], v0[2 * u + 1]);
+            sc[16 + u] = pack_b32x2(v1[2 * u], v1[2 * u + 1]);
           }
         }
         // this warpgroup's previous exchange slot was consumed long ago: hand it back (a
@@ -523,27 +547,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // the query half in tensor memory is free once the last score of its piece exists
         if (x.last && has_np) load_q_tmem(np.qb);
         const int valid = x.valid;
-        if (valid < kTileTok) {  // columns past the sequence end: sent as 0, masked below
-#pragma unroll
-          for (int j = 0; j < 64; ++j) sc[j] = (j < valid) ? sc[j] : 0.f;
-        }
+        if (valid < kTileTok) mask_pairs(sc, valid, 0.f);  // columns past the sequence end: sent as 0
         // ---- encode (16-bit block floating point, one exponent per 32 columns) and send
         {
           float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            a0 = fmaxf(a0, fabsf(sc[j]));
-            a1 = fmaxf(a1, fabsf(sc[j + 1]));
-            b0 = fmaxf(b0, fabsf(sc[32 + j]));
-            b1 = fmaxf(b1, fabsf(sc[32 + j + 1]));
+          for (int u = 0; u < 16; ++u) {
+            float x0, x1, y0, y1;
+            unpack_f32x2(sc[u], x0, x1);
+            unpack_f32x2(sc[16 + u], y0, y1);
+            a0 = fmaxf(a0, fabsf(x0));
+            a1 = fmaxf(a1, fabsf(x1));
+            b0 = fmaxf(b0, fabsf(y0));
+            b1 = fmaxf(b1, fabsf(y1));
           }
           const int e0 = bfp_exponent(fmaxf(a0, a1)), e1 = bfp_exponent(fmaxf(b0, b1));
-          const float k0 = pow2f(14 - e0), k1 = pow2f(14 - e1);
+          const uint64_t k0 = splat_f32x2(pow2f(14 - e0)), k1 = splat_f32x2(pow2f(14 - e1));
           uint32_t pk[32];
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
-            pk[u] = bfp_pack2_fast(sc[2 * u], sc[2 * u + 1], k0);
-            pk[16 + u] = bfp_pack2_fast(sc[32 + 2 * u], sc[32 + 2 * u + 1], k1);
+            pk[u] = bfp_pack_pair(sc[u], k0);
+            pk[16 + u] = bfp_pack_pair(sc[16 + u], k1);
           }
           if (!(ok = wait_warp(bar(B_X_FREE + sb), ph ^ 1, wc, kSiteXFree))) break;
           const uint32_t full = peer_bar0 + 8 * (B_X_FULL + sb);
@@ -559,7 +583,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint32_t pe;
           asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pe) : "r"(my_xe + r * 4));
           slot_dep = pe;
-          const float kp0 = pow2f((int)(int16_t)(pe & 0xFFFFu) - 14), kp1 = pow2f(((int)pe >> 16) - 14);
+          const uint64_t kp0 = splat_f32x2(pow2f((int)(int16_t)(pe & 0xFFFFu) - 14));
+          const uint64_t kp1 = splat_f32x2(pow2f(((int)pe >> 16) - 14));
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             uint32_t wv[4];
@@ -567,29 +592,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                          : "=r"(wv[0]), "=r"(wv[1]), "=r"(wv[2]), "=r"(wv[3])
                          : "r"(my_x + (j * kRows + r) * 16));
             slot_dep ^= wv[0] ^ wv[3];
-            const float kp = j < 4 ? kp0 : kp1;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              float q0, q1;
-              bfp_unpack2_fast(wv[u], q0, q1);
-              sc[8 * j + 2 * u] = fmaf(q0, kp, sc[8 * j + 2 * u]);
-              sc[8 * j + 2 * u + 1] = fmaf(q1, kp, sc[8 * j + 2 * u + 1]);
-            }
+            for (int q = 0; q < 4; ++q) sc[4 * j + q] = ffma_f32x2(bfp_unpack_pair(wv[q]), j < 4 ? kp0 : kp1, sc[4 * j + q]);
           }
         }
-        if (valid < kTileTok) {
+        if (valid < kTileTok) mask_pairs(sc, valid, -INFINITY);
+        float cm;
+        {
+          float c[4];
 #pragma unroll
-          for (int j = 0; j < 64; ++j) sc[j] = (j < valid) ? sc[j] : -INFINITY;
-        }
-        float c0 = sc[0], c1 = sc[1], c2 = sc[2], c3 = sc[3];
+          for (int q = 0; q < 4; ++q) {
+            float x0, x1;
+            unpack_f32x2(sc[q], x0, x1);
+            c[q] = fmaxf(x0, x1);
+          }
 #pragma unroll
-        for (int j = 4; j < 64; j += 4) {
-          c0 = fmaxf(c0, sc[j]);
-          c1 = fmaxf(c1, sc[j + 1]);
-          c2 = fmaxf(c2, sc[j + 2]);
-          c3 = fmaxf(c3, sc[j + 3]);
+          for (int u = 4; u < 32; ++u) {
+            float x0, x1;
+            unpack_f32x2(sc[u], x0, x1);
+            c[u & 3] = fmax3(c[u & 3], x0, x1);
+          }
+          cm = fmax3(c[0], c[1], fmaxf(c[2], c[3])) * sl2;  // log2 units (sl2 > 0)
         }
-        const float cm = fmaxf(fmaxf(c0, c1), fmaxf(c2, c3)) * sl2;  // log2 units (sl2 > 0)
         // ---- running max: decided from the previous tile's (the other warpgroup's)
         float m_prev = 0.f, l_other = 0.f;
         if (t > 0) {
@@ -608,24 +632,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float epi_l = 0.f;
         if (epi_pending) epi_l = l_other + (my_piece == epi_piece ? l_mine * exp2f(m_ref - m_prev) : 0.f);
         uint32_t pp[32];
-        float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+        float rsum;
+        {
+          const uint64_t s2 = splat_f32x2(sl2), nm = splat_f32x2(-m);
+          uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-        for (int u = 0; u < 32; u += 2) {
-          const float p0 = exp2f(fmaf(sc[2 * u], sl2, -m)), p1 = exp2f(fmaf(sc[2 * u + 1], sl2, -m));
-          const float p2 = exp2f(fmaf(sc[2 * u + 2], sl2, -m)), p3 = exp2f(fmaf(sc[2 * u + 3], sl2, -m));
-          pp[u] = pack_bf16(p0, p1);
-          pp[u + 1] = pack_bf16(p2, p3);
-          r0 += p0;
-          r1 += p1;
-          r2 += p2;
-          r3 += p3;
+          for (int u = 0; u < 32; ++u) {
+            float x0, x1;
+            unpack_f32x2(ffma_f32x2(sc[u], s2, nm), x0, x1);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            pp[u] = pack_bf16(p0, p1);
+            acc[u & 3] = fadd_f32x2(acc[u & 3], pack_f32x2(p0, p1));
+          }
+          float z[8];
+          unpack_f32x2(fadd_f32x2(fadd_f32x2(acc[0], acc[1]), fadd_f32x2(acc[2], acc[3])), z[0], z[1]);
+          rsum = z[0] + z[1];
         }
         if (piece != my_piece) {
           my_piece = piece;
           l_mine = 0.f;
           m_ref = m;
         }
-        l_mine = l_mine * exp2f(m_ref - m) + ((r0 + r1) + (r2 + r3));
+        l_mine = l_mine * exp2f(m_ref - m) + rsum;
         m_ref = m;
         ml[(sb * 2) * kRows + r] = m;
         ml[(sb * 2 + 1) * kRows + r] = l_mine;
