@@ -213,22 +213,25 @@ __device__ __forceinline__ void mask_pairs(uint64_t (&sc)[32], int valid, float 
   }
 }
 
-// Block floating point without conversion instructions.  Encode: x * 2^(14-e)
-// lies in (-2^14, 2^14); adding 1.5 * 2^23 in one FMA rounds it to an integer
-// (round to nearest even) held in the low mantissa bits, and the low 16 bits of
-// two such floats are packed into one word (two's-complement int16 each).
-// Decode: flip the sign bits (int16 -> offset binary u = v + 2^15), place u in
-// the mantissa of 2^23 (a float of value 2^23 + u) and subtract 2^23 + 2^15.
-// Both steps are exact.
+// Block floating point without conversion instructions, one exponent e per row
+// and tile (|x| < 2^e for every partial score x of the row).  Encode: n =
+// rint(x * 2^(14-e)) lies in [-2^14, 2^14]; adding 1.5 * 2^23 + 2^15 in one FMA
+// leaves n + 2^15 (offset binary) in the low 16 bits of the float, and two such
+// halves are packed into one word.  Decode: the half u placed in the mantissa of
+// 2^23 gives the float 2^23 + u = 2^23 + 2^15 + n, exactly; the receiver folds it
+// into its own partial with one FMA by kp = 2^(e_peer - 14), which leaves the
+// constant bias beta = (2^23 + 2^15) kp on every score of the row -- the softmax
+// only ever sees scores relative to the row max, so beta is removed there.
+constexpr float kBfpMagic = 12615680.0f;  // 1.5 * 2^23 + 2^15
+constexpr float kBfpBias = 8421376.0f;    // 2^23 + 2^15
 __device__ __forceinline__ uint32_t bfp_pack_pair(uint64_t xy, uint64_t k) {
   float a, b;
-  unpack_f32x2(ffma_f32x2(xy, k, splat_f32x2(12582912.0f)), a, b);
+  unpack_f32x2(ffma_f32x2(xy, k, splat_f32x2(kBfpMagic)), a, b);
   return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x5410);
 }
+// The two halves of w as the floats 2^23 + u.
 __device__ __forceinline__ uint64_t bfp_unpack_pair(uint32_t w) {
-  const uint32_t u = w ^ 0x80008000u;
-  return fadd_f32x2(pack_b32x2(__byte_perm(u, 0x4B000000u, 0x7410), __byte_perm(u, 0x4B000000u, 0x7432)),
-                    splat_f32x2(-8421376.0f));
+  return pack_b32x2(__byte_perm(w, 0x4B000000u, 0x7410), __byte_perm(w, 0x4B000000u, 0x7432));
 }
 
 __device__ __forceinline__ void st_async_b32(uint32_t cluster_dst, uint32_t v, uint32_t cluster_bar) {
@@ -527,6 +530,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!(ok = wait_warp(bar(B_S_FULL + sb), ph, wc, kSiteSFull))) break;
         tc_fence_after();
         uint64_t sc[32];  // score pairs: columns (2u, 2u + 1) in pair u
+        float beta = 0.f;  // bias the block-float decode leaves on every score of the row
         {
           uint32_t v0[32], v1[32];
           tmem_ld32(tmem + lane_off + TM_S + 64 * sb, v0);
@@ -550,31 +554,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (valid < kTileTok) mask_pairs(sc, valid, 0.f);  // columns past the sequence end: sent as 0
         // ---- encode (16-bit block floating point, one exponent per 32 columns) and send
         {
-          float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+          float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            float x0, x1, y0, y1;
+          for (int u = 0; u < 32; ++u) {
+            float x0, x1;
             unpack_f32x2(sc[u], x0, x1);
-            unpack_f32x2(sc[16 + u], y0, y1);
-            a0 = fmaxf(a0, fabsf(x0));
-            a1 = fmaxf(a1, fabsf(x1));
-            b0 = fmaxf(b0, fabsf(y0));
-            b1 = fmaxf(b1, fabsf(y1));
+            a[(2 * u) & 3] = fmaxf(a[(2 * u) & 3], fabsf(x0));
+            a[(2 * u + 1) & 3] = fmaxf(a[(2 * u + 1) & 3], fabsf(x1));
           }
-          const int e0 = bfp_exponent(fmaxf(a0, a1)), e1 = bfp_exponent(fmaxf(b0, b1));
-          const uint64_t k0 = splat_f32x2(pow2f(14 - e0)), k1 = splat_f32x2(pow2f(14 - e1));
+          const int e = bfp_exponent(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])));
+          const uint64_t k = splat_f32x2(pow2f(14 - e));
           uint32_t pk[32];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            pk[u] = bfp_pack_pair(sc[u], k0);
-            pk[16 + u] = bfp_pack_pair(sc[16 + u], k1);
-          }
+          for (int u = 0; u < 32; ++u) pk[u] = bfp_pack_pair(sc[u], k);
           if (!(ok = wait_warp(bar(B_X_FREE + sb), ph ^ 1, wc, kSiteXFree))) break;
           const uint32_t full = peer_bar0 + 8 * (B_X_FULL + sb);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             st_async_v4(peer_x + (j * kRows + r) * 16, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3], full);
-          st_async_b32(peer_xe + r * 4, ((uint32_t)e0 & 0xFFFFu) | ((uint32_t)e1 << 16), full);
+          st_async_b32(peer_xe + r * 4, (uint32_t)e, full);
         }
         // ---- the peer's half of the same scores
         if ((warp & 3) == 0 && lane == 0) mbar_arrive_expect_tx(bar(B_X_FULL + sb), kXBytes);
@@ -583,8 +581,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint32_t pe;
           asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pe) : "r"(my_xe + r * 4));
           slot_dep = pe;
-          const uint64_t kp0 = splat_f32x2(pow2f((int)(int16_t)(pe & 0xFFFFu) - 14));
-          const uint64_t kp1 = splat_f32x2(pow2f(((int)pe >> 16) - 14));
+          const float kpf = pow2f((int)pe - 14);
+          const uint64_t kp = splat_f32x2(kpf);
+          beta = kBfpBias * kpf;  // exact: a power of two times a 24-bit integer
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             uint32_t wv[4];
@@ -593,7 +592,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                          : "r"(my_x + (j * kRows + r) * 16));
             slot_dep ^= wv[0] ^ wv[3];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) sc[4 * j + q] = ffma_f32x2(bfp_unpack_pair(wv[q]), j < 4 ? kp0 : kp1, sc[4 * j + q]);
+            for (int q = 0; q < 4; ++q) sc[4 * j + q] = ffma_f32x2(bfp_unpack_pair(wv[q]), kp, sc[4 * j + q]);
           }
         }
         if (valid < kTileTok) mask_pairs(sc, valid, -INFINITY);
@@ -612,7 +611,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             unpack_f32x2(sc[u], x0, x1);
             c[u & 3] = fmax3(c[u & 3], x0, x1);
           }
-          cm = fmax3(c[0], c[1], fmaxf(c[2], c[3])) * sl2;  // log2 units (sl2 > 0)
+          cm = (fmax3(c[0], c[1], fmaxf(c[2], c[3])) - beta) * sl2;  // log2 units (sl2 > 0)
         }
         // ---- running max: decided from the previous tile's (the other warpgroup's)
         float m_prev = 0.f, l_other = 0.f;
@@ -634,7 +633,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t pp[32];
         float rsum;
         {
-          const uint64_t s2 = splat_f32x2(sl2), nm = splat_f32x2(-m);
+          const uint64_t s2 = splat_f32x2(sl2), nm = splat_f32x2(-fmaf(beta, sl2, m));
           uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
