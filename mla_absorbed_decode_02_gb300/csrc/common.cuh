@@ -76,8 +76,10 @@ __device__ __forceinline__ void drain_delay(uint64_t ns) {
 
 struct DecodeArgs {
   CUtensorMap map_qr;    // q^R half: bf16 {64, H, NQB}, box {32, 128, 1}, 64-byte swizzle
-  CUtensorMap map_kvc;   // latent of 64 cache rows: box {64 dims, 64 rows}, 128-byte swizzle
-  CUtensorMap map_kvr;   // RoPE key of 64 cache rows: box {32 dims, 64 rows}, 64-byte swizzle
+  CUtensorMap map_kvc;   // bf16 cache: latent of 64 rows, box {64 dims, 64 rows}, 128-byte swizzle;
+                         // FP8 cache (bytes): the 256 codes of one half, box {256, 64}, no swizzle
+  CUtensorMap map_kvr;   // RoPE key of 64 rows: bf16 box {32 dims, 64 rows} / bytes {64, 64}, 64-byte swizzle
+  CUtensorMap map_kvs;   // FP8 cache: the 4 tile scales of 64 rows, box {16 bytes, 64}, no swizzle
   const void* q_nope;    // absorbed queries, bf16 [NQB][H][512] (read by threads into tensor memory)
   const int32_t* block_table;
   const int32_t* seqlens;
@@ -87,7 +89,7 @@ struct DecodeArgs {
   float* o_acc;          // split partials [slots][H][512], normalised
   float* lse_acc;        // [slots][H]
   float scale_log2;      // softmax scale * log2(e)
-  int32_t H, s_q, causal, max_pages, out_f32, num_units, num_qb;
+  int32_t H, s_q, causal, max_pages, out_f32, num_units, num_qb, kv_fp8;
   uint64_t timeout_ns;
 };
 

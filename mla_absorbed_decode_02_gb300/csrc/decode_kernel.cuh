@@ -55,7 +55,12 @@ constexpr int kStages = 4;
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t kLatBlock = 8192;                  // [64 rows x 128 B]: 64 latent dims of a page
 constexpr uint32_t kStageRope = 4 * kLatBlock;        // RoPE half [64 rows x 64 B]
-constexpr uint32_t kStageBytes = kStageRope + 4096;   // 36 KB
+constexpr uint32_t kStageScales = kStageRope + 4096;  // FP8 cache: the 4 tile scales of 64 rows [64 x 16 B]
+constexpr uint32_t kStageBytes = kStageScales + 1024; // 37 KB
+// FP8 cache: this CTA's 256 E4M3 codes of 64 rows land row-major in the upper
+// half of the latent area and are expanded in place to the bf16 layout above.
+constexpr uint32_t kStageCodes = 2 * kLatBlock;
+constexpr uint32_t kFp8StageTx = 64 * 256 + 4096 + 1024;  // codes + RoPE half + scales
 constexpr uint32_t kPBytes = kRows * 128;             // one P buffer: [128 rows x 128 B] bf16, 128-byte swizzle
 constexpr uint32_t SM_P = kStages * kStageBytes;      // P[tile parity]
 constexpr uint32_t SM_QR = SM_P + 2 * kPBytes;        // RoPE-query half [128 x 64 B], 64-byte swizzle
@@ -79,7 +84,8 @@ enum : uint32_t {
   B_DRAIN_PV,
   B_KV_FULL,                        // + stage
   B_KV_EMPTY = B_KV_FULL + kStages,
-  B_S_FULL = B_KV_EMPTY + kStages,  // [parity] QK(t) done
+  B_K_READY = B_KV_EMPTY + kStages, // + stage: FP8 cache expanded to bf16
+  B_S_FULL = B_K_READY + kStages,   // [parity] QK(t) done
   B_S_EMPTY = B_S_FULL + 2,         // [parity] scores of tile t read out
   B_P_FULL = B_S_EMPTY + 2,         // [parity] P(t) written
   B_P_FREE = B_P_FULL + 2,          // [parity] PV(t) done
@@ -240,6 +246,39 @@ __device__ __forceinline__ void st_async_b32(uint32_t cluster_dst, uint32_t v, u
                : "memory");
 }
 
+// FP8 cache: this warpgroup thread's share of a stage (i in [0, 128): row i/2, the 128 codes of tile
+// half i%2) -> bf16 x tile scale, written into the 128-byte-swizzled latent layout the MMAs read.
+// The codes sit in the upper half of the latent area, so every thread of the warpgroup reads its codes
+// before any thread writes (named barrier bar_id over the 128 threads).
+__device__ __forceinline__ void expand_fp8_stage(uint32_t sbase, int i, uint32_t half, uint32_t bar_id) {
+  const int row = i >> 1, part = i & 1;
+  uint32_t c[32];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(c[4 * j]), "=r"(c[4 * j + 1]), "=r"(c[4 * j + 2]), "=r"(c[4 * j + 3])
+                 : "r"(sbase + kStageCodes + row * 256 + part * 128 + 16 * j));
+  float scale;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(scale) : "r"(sbase + kStageScales + row * 16 + (2 * half + part) * 4));
+  asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+#pragma unroll
+  for (int ch = 0; ch < 16; ++ch) {  // 8 codes -> 8 bf16 (16 bytes)
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint16_t two = (uint16_t)(c[2 * ch + (q >> 1)] >> (16 * (q & 1)));
+      uint32_t h2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+      o[q] = pack_bf16(f.x * scale, f.y * scale);
+    }
+    const int blk = 2 * part + (ch >> 3), chunk = ch & 7;
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sbase + blk * kLatBlock + row * 128 +
+                                                              ((((uint32_t)chunk) ^ (row & 7)) << 4)),
+                 "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]));
+  }
+}
+
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
@@ -282,6 +321,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(B_KV_FULL + s), 1);
       mbar_init(bar(B_KV_EMPTY + s), 1);
+      mbar_init(bar(B_K_READY + s), 4);  // the four warps of the warpgroup that expands the stage
     }
     for (int p = 0; p < 2; ++p) {
       mbar_init(bar(B_S_FULL + p), 1);   // MMA commit
@@ -327,6 +367,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&args.map_qr);
       prefetch_tensormap(&args.map_kvc);
       prefetch_tensormap(&args.map_kvr);
+      if (args.kv_fp8) prefetch_tensormap(&args.map_kvs);
       const uint64_t pol_kv = l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
       TileCursor cur;
@@ -342,14 +383,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         const uint32_t st = t % kStages, ph = (t / kStages) & 1;
         if (!wait_one(bar(B_KV_EMPTY + st), ph ^ 1, wc, kSiteKvEmpty)) break;
-        mbar_arrive_expect_tx(bar(B_KV_FULL + st), kStageBytes);
         const int b = ti.qb / args.s_q;
         const int page = args.block_table[(int64_t)b * args.max_pages + ti.tile];
         const uint32_t sbase = base + st * kStageBytes;
-        for (int blk = 0; blk < 4; ++blk)
-          tma_load_2d(sbase + blk * kLatBlock, &args.map_kvc, bar(B_KV_FULL + st), 256 * half + 64 * blk, page * 64,
-                      pol_kv);
-        tma_load_2d(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 512 + 32 * half, page * 64, pol_kv);
+        if (args.kv_fp8) {  // 656-byte rows: codes of this half, its RoPE half, the 4 tile scales
+          mbar_arrive_expect_tx(bar(B_KV_FULL + st), kFp8StageTx);
+          tma_load_2d(sbase + kStageCodes, &args.map_kvc, bar(B_KV_FULL + st), 256 * half, page * 64, pol_kv);
+          tma_load_2d(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 528 + 64 * half, page * 64, pol_kv);
+          tma_load_2d(sbase + kStageScales, &args.map_kvs, bar(B_KV_FULL + st), 512, page * 64, pol_kv);
+        } else {
+          mbar_arrive_expect_tx(bar(B_KV_FULL + st), kStageBytes - 1024);
+          for (int blk = 0; blk < 4; ++blk)
+            tma_load_2d(sbase + blk * kLatBlock, &args.map_kvc, bar(B_KV_FULL + st), 256 * half + 64 * blk, page * 64,
+                        pol_kv);
+          tma_load_2d(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 512 + 32 * half, page * 64, pol_kv);
+        }
         ++t;
       }
     }
@@ -373,7 +421,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ++piece_no;
           }
           const uint32_t st = t % kStages, sb = t & 1;
-          if (!wait_one(bar(B_KV_FULL + st), (t / kStages) & 1, wc, kSiteKvFull)) break;
+          if (!wait_one(bar((args.kv_fp8 ? B_K_READY : B_KV_FULL) + st), (t / kStages) & 1, wc, kSiteKvFull)) break;
           if (!wait_one(bar(B_S_EMPTY + sb), ((t >> 1) & 1) ^ 1, wc, kSiteSEmpty)) break;
           tc_fence_after();
           const uint32_t sbase = base + st * kStageBytes;
@@ -514,6 +562,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     float l_mine = 0.f, m_ref = 0.f;  // this warpgroup's part of the row sum, relative to m_ref
     uint32_t slot_dep = 0;            // computed from the last values read from the exchange slot
     int my_piece = -1;                // piece that l_mine belongs to
+    // FP8 cache: the warpgroup of tile t expands stage t to bf16 -- its first tile up front, tile
+    // t + 2 right after publishing P(t) -- so QK(t) finds a bf16 page.
+    uint32_t n_tiles = 0;  // tiles of this unit
+    {
+      PieceWalker pw = walker0;
+      Piece pc;
+      while (pw.next(pc)) n_tiles += pc.t1 - pc.t0;
+    }
+    auto expand_tile = [&](uint32_t tt) -> bool {
+      const uint32_t st = tt % kStages;
+      if (!wait_warp(bar(B_KV_FULL + st), (tt / kStages) & 1, wc, kSiteKvFull)) return false;
+      expand_fp8_stage(base + st * kStageBytes, r, half, 1 + w);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_K_READY + st));
+      return true;
+    };
+    if (args.kv_fp8 && w < n_tiles) ok = expand_tile(w);
     TileCursor cursor;
     cursor.init(walker0);
     TileInfo x;
@@ -701,6 +767,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_P_FULL + sb));
+        if (args.kv_fp8 && t + 2 < n_tiles && !(ok = expand_tile(t + 2))) break;
       }
       if (x.last) {  // the warpgroup of the next tile finishes this piece
         epi_qb = x.qb;

@@ -264,7 +264,6 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
   for (const void* q : ptrs)
     if (!q || !aligned16(q)) return MLA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return MLA_ERR_INVALID_ARG;  // the kernel takes row maxima before scaling
-  if (p->kv_dtype != MLA_KV_BF16) return MLA_ERR_UNSUPPORTED;
   DeviceInfo* dinfo = nullptr;
   if ((st = device_info(&dinfo)) != MLA_OK) return st;
   int32_t U = 0;
@@ -281,7 +280,7 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
     if ((st = encode_map(&a.map_qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_rope, d, s, bx, CU_TENSOR_MAP_SWIZZLE_64B)))
       return st;
   }
-  {
+  if (p->kv_dtype == MLA_KV_BF16) {
     const uint64_t d[2] = {576, (uint64_t)p->num_pages * 64};
     const uint64_t s[1] = {576 * 2};
     const uint32_t bc[2] = {64, 64}, br[2] = {32, 64};
@@ -291,7 +290,19 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
     if ((st = encode_map(&a.map_kvr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_pages, d, s, br,
                          CU_TENSOR_MAP_SWIZZLE_64B)))
       return st;
+    a.map_kvs = a.map_kvr;  // unused
+  } else {  // FP8 rows of 656 bytes: 512 codes, 4 float32 scales, 64 bf16 RoPE
+    const uint64_t d[2] = {656, (uint64_t)p->num_pages * 64};
+    const uint64_t s[1] = {656};
+    const uint32_t bc[2] = {256, 64}, br[2] = {64, 64}, bs[2] = {16, 64};
+    if ((st = encode_map(&a.map_kvc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_pages, d, s, bc, CU_TENSOR_MAP_SWIZZLE_NONE)))
+      return st;
+    if ((st = encode_map(&a.map_kvr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_pages, d, s, br, CU_TENSOR_MAP_SWIZZLE_64B)))
+      return st;
+    if ((st = encode_map(&a.map_kvs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_pages, d, s, bs, CU_TENSOR_MAP_SWIZZLE_NONE)))
+      return st;
   }
+  a.kv_fp8 = p->kv_dtype == MLA_KV_FP8_E4M3;
   a.q_nope = q_nope_absorbed;
   a.block_table = block_table;
   a.seqlens = cache_seqlens;

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import mla_workloads as mw
-from gpu_util import BF16_TOL, compare, oracle_full, oracle_sampled, run_gpu, to_device, params_for
+from gpu_util import BF16_TOL, FP8_TOL, compare, oracle_full, oracle_sampled, run_gpu, to_device, params_for
 
 pytestmark = pytest.mark.gpu
 
@@ -40,7 +40,7 @@ def test_workload_tiny_full():
     print("tiny", errs)
 
 
-@pytest.mark.parametrize("index", [1, 2, 3])
+@pytest.mark.parametrize("index", [1, 2, 3, 4])
 def test_workload_full_size_sampled(index):
     w = mw.make_workload(index)
     out, lse, _ = run_gpu(w)
@@ -58,7 +58,7 @@ def test_workload_full_size_sampled(index):
         ref_o.append(o)
         ref_l.append(l)
     errs = compare(np.concatenate(got_o), np.concatenate(got_l), np.concatenate(ref_o), np.concatenate(ref_l),
-                   BF16_TOL, w.name, out_bf16=True)
+                   FP8_TOL if w.kv_dtype == "fp8" else BF16_TOL, w.name, out_bf16=True)
     print(w.name, errs)
 
 
@@ -131,6 +131,29 @@ def test_long_tail_row_garbage_is_ignored():
         page = w.block_table[b, last]
         w.kv[page, int(L) % 64 or 64:, :] = nan_bf16
     full_check(w, num_units=2, what="NaN past the end")
+
+
+# ------------------------------------------------------------------ FP8 E4M3 latent cache
+
+@pytest.mark.parametrize("num_units", [0, 3])
+def test_fp8_cache_ragged(num_units):
+    w = mw.make_custom([1, 64, 65, 300, 1000, 2049], num_heads=128, kv_dtype="fp8", seed=21, pool_factor=1.2)
+    errs = full_check(w, tol=FP8_TOL, num_units=num_units, what=f"fp8 U={num_units}")
+    print("fp8", errs)
+
+
+def test_fp8_two_new_tokens_causal():
+    w = mw.make_custom([2, 129, 700], num_heads=128, s_q=2, causal=True, kv_dtype="fp8", seed=22)
+    full_check(w, tol=FP8_TOL, num_units=4, what="fp8 s_q=2")
+
+
+def test_fp8_row_garbage_past_the_end_is_ignored():
+    """FP8 rows past the sequence end hold NaN codes, NaN scales and NaN RoPE: they must not leak."""
+    w = mw.make_custom([65, 130, 1], num_heads=64, kv_dtype="fp8", seed=23)
+    for b, L in enumerate(w.seqlens):
+        page = w.block_table[b, (int(L) - 1) // 64]
+        w.kv[page, int(L) % 64 or 64:, :] = 0xFF
+    full_check(w, tol=FP8_TOL, num_units=2, what="fp8 NaN past the end")
 
 
 # ------------------------------------------------------------------ metadata, errors
