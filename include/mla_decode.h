@@ -160,6 +160,20 @@ int32_t mla_plan_host(const mla_decode_params* p, int32_t num_units, const int32
 int32_t mla_resolve_num_units(const mla_decode_params* p, int32_t* num_units);
 
 /*
+ * Writes the FP8 form of a bf16 cache ("MLA and FP8 MoE Serving: Multi-Head Latent
+ * Attention at Scale", section "Understanding FP8 Formats: E4M3 vs. E5M2"; "MLA inference:
+ * two computation paths and FlashMLA", exercise 2 "An FP8 KV Cache"), in the layout
+ * MLA_KV_FP8_E4M3 reads.
+ *   kv_bf16   device bf16 [num_tokens][576]: latent c (512) then k^R (64)
+ *   kv_fp8    device [num_tokens][656 bytes]: 512 E4M3 codes, 4 float32 scales (one per
+ *             128-element latent tile), the 64 bf16 RoPE values copied unchanged
+ * Per tile: scale = amax / 448 (1 for an all-zero tile); code = E4M3(clamp(x / scale,
+ * -448, 448)) rounded to nearest even; the decoded value is code * scale.  num_tokens = 0
+ * launches nothing.  Both buffers 16-byte aligned; asynchronous on stream.
+ */
+int32_t mla_quantize_kv_fp8(const void* kv_bf16, void* kv_fp8, int64_t num_tokens, void* stream);
+
+/*
  * Device error word of the current device: synchronises the device, writes the
  * word to *word (MLA_OK if none; MLA_ERR_TIMEOUT + 16 * site otherwise) and,
  * if clear != 0, resets it.  Host pointer.

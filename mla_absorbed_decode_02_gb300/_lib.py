@@ -71,6 +71,7 @@ def load_library():
             "mla_device_error": ([ctypes.POINTER(i32), i32], i32),
             "mla_wait_selftest": ([i32, vp], i32),
             "mla_decode_noalloc": ([P, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp], i32),
+            "mla_quantize_kv_fp8": ([vp, vp, ctypes.c_int64, vp], i32),
             "mla_status_string": ([i32], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -164,6 +165,12 @@ def mla_decode_noalloc(p: MlaDecodeParams, q_nope_absorbed, q_rope, kv_pages, bl
     _check(load_library().mla_decode_noalloc(ctypes.byref(p), _ptr(q_nope_absorbed), _ptr(q_rope), _ptr(kv_pages),
                                              _ptr(block_table), _ptr(cache_seqlens), float(scale), _ptr(out),
                                              _ptr(lse), _stream(stream)), "mla_decode_noalloc")
+
+
+def mla_quantize_kv_fp8(kv_bf16, kv_fp8, num_tokens: int, stream=None):
+    """bf16 cache rows [n, 576] -> 656-byte FP8 rows [n, 656] (codes, tile scales, RoPE)."""
+    _check(load_library().mla_quantize_kv_fp8(_ptr(kv_bf16), _ptr(kv_fp8), int(num_tokens), _stream(stream)),
+           "mla_quantize_kv_fp8")
 
 
 def mla_device_error(clear: bool = True) -> int:

@@ -2,6 +2,7 @@
 // the decode kernel -- split planning, LSE combine, bounded-wait self test.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -76,6 +77,49 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const int32_t* sched, 
     *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + row * 512 + d) = o;
   }
   if (threadIdx.x == 0) lse[row] = L;
+}
+
+// ----------------------------------------------------------------- FP8 cache writer
+// bf16 rows [576] (latent 512 + RoPE 64) -> 656-byte FP8 rows: 512 E4M3 codes, the 4
+// float32 tile scales, the 64 bf16 RoPE values unchanged.  Per 128-element tile:
+// scale = amax / 448 (1 if the tile is all zero), code = E4M3(x / scale) rounded to
+// nearest even, the quotient first clamped to the E4M3 range +-448 ("MLA and FP8 MoE
+// Serving: Multi-Head Latent Attention at Scale", section "Understanding FP8 Formats:
+// E4M3 vs. E5M2").  One warp per token; lane l owns latent elements [16 l, 16 l + 16),
+// so a tile is 8 lanes.
+__global__ void __launch_bounds__(256) mla_quantize_fp8_kernel(const __nv_bfloat16* kv, uint8_t* out, int64_t n) {
+  const int64_t tok = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (tok >= n) return;
+  const __nv_bfloat16* src = kv + tok * 576;
+  uint8_t* dst = out + tok * 656;
+  float x[16];
+  {
+    const uint4 a = *reinterpret_cast<const uint4*>(src + 16 * lane);
+    const uint4 b = *reinterpret_cast<const uint4*>(src + 16 * lane + 8);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float scale = amax > 0.f ? amax / 448.f : 1.f;
+  uint32_t codes[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float y = fminf(fmaxf(x[i] / scale, -448.f), 448.f);
+    const uint32_t c = (uint32_t)__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+    codes[i >> 2] |= c << (8 * (i & 3));
+  }
+  *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+  if ((lane & 7) == 0) *reinterpret_cast<float*>(dst + 512 + 4 * (lane >> 3)) = scale;
+  if (lane < 8) *reinterpret_cast<uint4*>(dst + 528 + 16 * lane) = *reinterpret_cast<const uint4*>(src + 512 + 8 * lane);
 }
 
 // ----------------------------------------------------------------- bounded-wait self test
@@ -369,6 +413,16 @@ int32_t mla_device_error(int32_t* word, int32_t clear) {
     if (cudaMemcpyToSymbol(g_mla_error, &z, sizeof z) != cudaSuccess) return MLA_ERR_CUDA;
   }
   return MLA_OK;
+}
+
+int32_t mla_quantize_kv_fp8(const void* kv_bf16, void* kv_fp8, int64_t num_tokens, void* stream) {
+  if (!kv_bf16 || !kv_fp8 || num_tokens < 0 || !aligned16(kv_bf16) || !aligned16(kv_fp8)) return MLA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return MLA_OK;
+  const int64_t blocks = (num_tokens + 7) / 8;
+  if (blocks > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  mla_quantize_fp8_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(kv_bf16), static_cast<uint8_t*>(kv_fp8), num_tokens);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 int32_t mla_wait_selftest(int32_t timeout_us, void* stream) {
