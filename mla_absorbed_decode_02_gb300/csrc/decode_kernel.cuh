@@ -50,23 +50,29 @@ namespace mla {
 constexpr int kThreads = 384;
 constexpr int kRows = 128;      // MMA M: head rows (H <= 128, padded with zero queries)
 constexpr int kTileTok = 64;    // tokens per work tile (one page)
-constexpr int kStages = 4;
+#ifndef MLA_STAGES
+#define MLA_STAGES 5
+#endif
+constexpr int kStages = MLA_STAGES;
 
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t kLatBlock = 8192;                  // [64 rows x 128 B]: 64 latent dims of a page
 constexpr uint32_t kStageRope = 4 * kLatBlock;        // RoPE half [64 rows x 64 B]
-constexpr uint32_t kStageScales = kStageRope + 4096;  // FP8 cache: the 4 tile scales of 64 rows [64 x 16 B]
-constexpr uint32_t kStageBytes = kStageScales + 1024; // 37 KB
+constexpr uint32_t kStageBytes = kStageRope + 4096;   // 36 KB
 // FP8 cache: this CTA's 256 E4M3 codes of 64 rows land row-major in the upper
-// half of the latent area and are expanded in place to the bf16 layout above.
+// half of the latent area, the 4 tile scales of the 64 rows [64 x 16 B] at its
+// start; both are read before the expansion to the bf16 layout overwrites them.
 constexpr uint32_t kStageCodes = 2 * kLatBlock;
+constexpr uint32_t kStageScales = 0;
 constexpr uint32_t kFp8StageTx = 64 * 256 + 4096 + 1024;  // codes + RoPE half + scales
-constexpr uint32_t kPBytes = kRows * 128;             // one P buffer: [128 rows x 128 B] bf16, 128-byte swizzle
-constexpr uint32_t SM_P = kStages * kStageBytes;      // P[tile parity]
+constexpr uint32_t kBf16StageTx = 4 * kLatBlock + 4096;   // latent half + RoPE half
+// P / exchange buffer of a tile parity: the peer's partial scores of tile t arrive here
+// ([8][128 rows][16 B]), are decoded, and P(t) ([128 rows x 128 B] bf16, 128-byte
+// swizzle) is written over them; the buffer is handed back to the peer once PV(t) is done.
+constexpr uint32_t kPBytes = kRows * 128;
+constexpr uint32_t SM_P = kStages * kStageBytes;      // P / exchange [tile parity]
 constexpr uint32_t SM_QR = SM_P + 2 * kPBytes;        // RoPE-query half [128 x 64 B], 64-byte swizzle
-constexpr uint32_t kXSlot = 8 * kRows * 16;           // peer partial scores of one tile: [8][128 rows][16 B]
-constexpr uint32_t SM_X = SM_QR + 8192;               // exchange slots [tile parity]
-constexpr uint32_t SM_XE = SM_X + 2 * kXSlot;         // peer exponent pairs [tile parity][128 rows] u32
+constexpr uint32_t SM_XE = SM_QR + 8192;              // peer block-float exponents [tile parity][128 rows] u32
 constexpr uint32_t SM_ML = SM_XE + 2 * kRows * 4;     // published running max / row sum: [parity][2][128] f32
 constexpr uint32_t SM_BAR = SM_ML + 2 * 2 * kRows * 4;
 constexpr uint32_t kSmemBytes = SM_BAR + 512 + 1024;  // + alignment slack
@@ -392,7 +398,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tma_load_2d(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 528 + 64 * half, page * 64, pol_kv);
           tma_load_2d(sbase + kStageScales, &args.map_kvs, bar(B_KV_FULL + st), 512, page * 64, pol_kv);
         } else {
-          mbar_arrive_expect_tx(bar(B_KV_FULL + st), kStageBytes - 1024);
+          mbar_arrive_expect_tx(bar(B_KV_FULL + st), kBf16StageTx);
           for (int blk = 0; blk < 4; ++blk)
             tma_load_2d(sbase + blk * kLatBlock, &args.map_kvc, bar(B_KV_FULL + st), 256 * half + 64 * blk, page * 64,
                         pol_kv);
@@ -472,9 +478,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int r = ((warp & 3) << 5) | lane;        // head row == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t peer_bar0 = map_to_rank(bar(0), peer);  // the peer's barrier i is at peer_bar0 + 8 i
-    const uint32_t peer_x = map_to_rank(base + SM_X + w * kXSlot, peer);
+    const uint32_t peer_x = map_to_rank(base + SM_P + w * kPBytes, peer);
     const uint32_t peer_xe = map_to_rank(base + SM_XE + w * kRows * 4, peer);
-    const uint32_t my_x = base + SM_X + w * kXSlot, my_xe = base + SM_XE + w * kRows * 4;
+    const uint32_t my_x = base + SM_P + w * kPBytes, my_xe = base + SM_XE + w * kRows * 4;
     float* ml = reinterpret_cast<float*>(smem + SM_ML);  // [parity][0 = max, 1 = row sum][128]
     const float sl2 = args.scale_log2;
     const int H = args.H;
@@ -611,9 +617,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             sc[16 + u] = pack_b32x2(v1[2 * u], v1[2 * u + 1]);
           }
         }
-        // this warpgroup's previous exchange slot was consumed long ago: hand it back (a
-        // relaxed arrive, made to depend on the values read from the slot)
-        if (t >= 2 && lane == 0) mbar_arrive_remote_relaxed(peer_bar0 + 8 * (B_X_FREE + sb), slot_dep);
+        // this warpgroup's buffer held P(t-2): hand it back to the peer once PV(t-2) is done
+        // (a relaxed arrive, made to depend on the values read from the buffer)
+        if (t >= 2) {
+          if (!(ok = wait_warp(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) break;
+          if (lane == 0) mbar_arrive_remote_relaxed(peer_bar0 + 8 * (B_X_FREE + sb), slot_dep);
+        }
         // the query half in tensor memory is free once the last score of its piece exists
         if (x.last && has_np) load_q_tmem(np.qb);
         const int valid = x.valid;
@@ -746,8 +755,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_wait_st();
           }
         }
-        // ---- publish P (its buffer is free once PV(t-2) is done)
-        if (!(ok = wait_warp(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) break;
+        // ---- publish P over the decoded exchange data (PV(t-2) was waited for above); every
+        // thread of the warpgroup has read its rows of the exchange data before any P row lands
+        asm volatile("bar.sync %0, 128;" ::"r"(1 + w) : "memory");
         if (valid < kTileTok) {
           // rows past the sequence end must not reach the PV product (0 * garbage): zero them
           const uint32_t sbase = base + (t % kStages) * kStageBytes;
