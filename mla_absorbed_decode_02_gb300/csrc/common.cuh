@@ -81,6 +81,7 @@ struct DecodeArgs {
   CUtensorMap map_kvr;   // RoPE key of 64 rows: bf16 box {32 dims, 64 rows} / bytes {64, 64}, 64-byte swizzle
   CUtensorMap map_kvs;   // FP8 cache: the 4 tile scales of 64 rows, box {16 bytes, 64}, no swizzle
   const void* q_nope;    // absorbed queries, bf16 [NQB][H][512] (read by threads into tensor memory)
+  const void* q_rope;    // RoPE queries, bf16 [NQB][H][64] (loaded by TMA; read here only to prefetch into L2)
   const int32_t* block_table;
   const int32_t* seqlens;
   const int32_t* sched;

@@ -487,22 +487,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     // absorbed-query half of query block qb -> tensor memory (A operand of the latent score)
+    // (all 32 row loads in flight at once: one memory latency)
     auto load_q_tmem = [&](int qb) {
       const uint32_t* src = reinterpret_cast<const uint32_t*>(args.q_nope) + ((int64_t)qb * H + r) * 256 + 128 * half;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t q[32];
+      uint32_t q[128];
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (r < H) v = *reinterpret_cast<const uint4*>(src + 32 * c + j);
-          q[j] = v.x;
-          q[j + 1] = v.y;
-          q[j + 2] = v.z;
-          q[j + 3] = v.w;
-        }
-        tmem_st32(tmem + lane_off + TM_Q + 32 * c, q);
+      for (int j = 0; j < 128; j += 4) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < H) v = *reinterpret_cast<const uint4*>(src + j);
+        q[j] = v.x;
+        q[j + 1] = v.y;
+        q[j + 2] = v.z;
+        q[j + 3] = v.w;
       }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_st32(tmem + lane_off + TM_Q + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(q + 32 * c));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -595,12 +594,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (x.first) {
         ++piece;
         has_np = ahead.next(np);  // the piece after this one
+        if (has_np && (t & 1) == w && r < H) {  // bring its query rows into L2 for the load at this piece's end
+          const char* qn = reinterpret_cast<const char*>(args.q_nope) + (((int64_t)np.qb * H + r) * 512 + 256 * half) * 2;
+          const char* qr = reinterpret_cast<const char*>(args.q_rope) + (((int64_t)np.qb * H + r) * 64 + 32 * half) * 2;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + 128 * k));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(qr));
+        }
       }
       if ((t & 1) == w) {
         const uint32_t sb = w, ph = (t >> 1) & 1;
         // ---- own partial scores; the score buffer is free again right after the read
         if (!(ok = wait_warp(bar(B_S_FULL + sb), ph, wc, kSiteSFull))) break;
         tc_fence_after();
+        // QK(t) is done: if it was the piece's last, the query half in tensor memory is free
+        if (x.last && has_np) load_q_tmem(np.qb);
         uint64_t sc[32];  // score pairs: columns (2u, 2u + 1) in pair u
         float beta = 0.f;  // bias the block-float decode leaves on every score of the row
         {
@@ -623,8 +631,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!(ok = wait_warp(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) break;
           if (lane == 0) mbar_arrive_remote_relaxed(peer_bar0 + 8 * (B_X_FREE + sb), slot_dep);
         }
-        // the query half in tensor memory is free once the last score of its piece exists
-        if (x.last && has_np) load_q_tmem(np.qb);
         const int valid = x.valid;
         if (valid < kTileTok) mask_pairs(sc, valid, 0.f);  // columns past the sequence end: sent as 0
         // ---- encode (16-bit block floating point, one exponent per 32 columns) and send

@@ -348,6 +348,7 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
   }
   a.kv_fp8 = p->kv_dtype == MLA_KV_FP8_E4M3;
   a.q_nope = q_nope_absorbed;
+  a.q_rope = q_rope;
   a.block_table = block_table;
   a.seqlens = cache_seqlens;
   a.sched = static_cast<const int32_t*>(sched);
