@@ -25,9 +25,13 @@ constexpr int kSchedHeader = 8;               // int32 header words
 constexpr int kUnitInts = 8;                  // int32 words per unit record
 constexpr int kTile = 64;                     // tokens per work tile (one page)
 // Cost of one piece of work beyond its tiles, in tile units: loading the
-// 128 x 288 query half and writing the 128 x 256 output half (about two
-// tiles' worth of bytes, mostly served by L2).
-constexpr int kPieceFixedCost = 2;
+// 128 x 288 query half, the epilogue writing the 128 x 256 output half, and the
+// pipeline refill between pieces -- measured at about six tiles' time per piece
+// boundary on GB300 (the plan balances positions, so this is what evens the units).
+#ifndef MLA_PIECE_COST
+#define MLA_PIECE_COST 6
+#endif
+constexpr int kPieceFixedCost = MLA_PIECE_COST;
 
 MLA_HD inline int32_t visible_keys(int32_t L, int s_q, int t, int causal) {
   int32_t n = causal ? L - s_q + 1 + t : L;

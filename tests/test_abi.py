@@ -85,7 +85,8 @@ def test_reserved_must_be_zero(lib):
 # ------------------------------------------------------------------ split planner
 
 TILE = 64
-FIX = 2
+FIX = int(re.search(r"#define MLA_PIECE_COST (\d+)", open(os.path.join(os.path.dirname(os.path.dirname(
+    os.path.abspath(__file__))), "mla_absorbed_decode_02_gb300", "csrc", "plan.h")).read()).group(1))
 
 
 def visible(L, s_q, t, causal):
