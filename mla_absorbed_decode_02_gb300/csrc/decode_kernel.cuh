@@ -309,6 +309,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (tid == 0) atomicCAS(&g_mla_error, 0, 5);
     return;
   }
+  pdl_launch_dependents();  // the combine kernel may start launching; it waits for this grid to finish
   const int32_t* rec = sched + kSchedHeader + kUnitInts * unit;
   if (rec[0] < 0) return;  // no work for this unit (both CTAs take this path)
   const int32_t* num_splits = sched + kSchedHeader + kUnitInts * args.num_units;
@@ -511,6 +512,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // epilogue of a finished piece: O / l -> out (or a split partial), lse
     int epi_qb = 0, epi_split = 0, epi_piece = -1;
     bool epi_pending = false;
+    const uint64_t pol_partial = l2_policy_evict_last();
     auto epilogue = [&](float m_fin, float l_tot) {
       const bool split = num_splits[epi_qb] > 1;
       const int slot = split ? split_offset[epi_qb] + epi_split : 0;
@@ -530,10 +532,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               float* dst = split ? args.o_acc + ((int64_t)slot * H + r) * 512 + d0
                                  : reinterpret_cast<float*>(args.out) + ((int64_t)epi_qb * H + r) * 512 + d0;
 #pragma unroll
-              for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(dst + j) =
-                    make_float4(__uint_as_float(v[h2][j]) * inv_l, __uint_as_float(v[h2][j + 1]) * inv_l,
-                                __uint_as_float(v[h2][j + 2]) * inv_l, __uint_as_float(v[h2][j + 3]) * inv_l);
+              for (int j = 0; j < 32; j += 4) {
+                const float4 o4 = make_float4(__uint_as_float(v[h2][j]) * inv_l, __uint_as_float(v[h2][j + 1]) * inv_l,
+                                              __uint_as_float(v[h2][j + 2]) * inv_l, __uint_as_float(v[h2][j + 3]) * inv_l);
+                if (split)  // read back by the combine right after this kernel: keep it in L2
+                  st_global_v4_hint(dst + j, o4, pol_partial);
+                else
+                  *reinterpret_cast<float4*>(dst + j) = o4;
+              }
             } else {
               __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.out) + ((int64_t)epi_qb * H + r) * 512 + d0;
 #pragma unroll

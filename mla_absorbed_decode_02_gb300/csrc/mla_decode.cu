@@ -44,6 +44,7 @@ __global__ void __launch_bounds__(1024) mla_sched_kernel(const int32_t* seqlens,
 __global__ void __launch_bounds__(128) mla_combine_kernel(const int32_t* sched, int U, int NQB, int H,
                                                           const float* o_acc, const float* lse_acc, void* out,
                                                           float* lse, int out_f32) {
+  pdl_wait_prerequisites();  // the decode kernel before it in the stream has finished
   const int qb = blockIdx.x, h = blockIdx.y, d = threadIdx.x * 4;
   const int32_t* num_splits = sched + kSchedHeader + kUnitInts * U;
   const int32_t* split_offset = num_splits + NQB;
@@ -61,7 +62,7 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const int32_t* sched, 
     L = M + logf(S);
     for (int i = 0; i < ns; ++i) {
       const float wgt = expf(lse_acc[(int64_t)(off + i) * H + h] - L);
-      const float4 v = *reinterpret_cast<const float4*>(o_acc + ((int64_t)(off + i) * H + h) * 512 + d);
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(o_acc + ((int64_t)(off + i) * H + h) * 512 + d));
       acc[0] += wgt * v.x;
       acc[1] += wgt * v.y;
       acc[2] += wgt * v.z;
@@ -389,9 +390,22 @@ int32_t mla_combine(const mla_decode_params* p, void* out, float* lse, const voi
   const float* o_acc = static_cast<const float*>(workspace);
   const float* lse_acc =
       reinterpret_cast<const float*>(static_cast<const char*>(workspace) + align256(slots * H * 512 * sizeof(float)));
-  mla_combine_kernel<<<dim3(NQB, H, 1), 128, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const int32_t*>(sched), U, NQB, H, o_acc, lse_acc, out, lse, p->out_dtype == MLA_OUT_F32);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  // programmatic dependent launch: this grid is set up while the decode kernel before it
+  // drains, and waits (griddepcontrol.wait) for it before reading the partials
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(NQB, H, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_combine_kernel, static_cast<const int32_t*>(sched), U, NQB, H, o_acc, lse_acc,
+                            out, lse, (int)(p->out_dtype == MLA_OUT_F32)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 int32_t mla_decode(const mla_decode_params* p, const void* q_nope_absorbed, const void* q_rope, const void* kv_pages,

@@ -133,6 +133,27 @@ def test_long_tail_row_garbage_is_ignored():
     full_check(w, num_units=2, what="NaN past the end")
 
 
+def test_metadata_is_reusable_across_calls():
+    """One scheduler metadata serves every call of a step: two decodes with the same
+    metadata and workspace give the same bits (and the oracle's result)."""
+    import torch
+    from mla_absorbed_decode_02_gb300 import Decoder, mla_device_error
+    w = mw.make_custom([3000, 40, 5000, 700, 1], num_heads=128, seed=24)
+    q_nope, q_rope, kv, bt, seq = to_device(w)
+    dec = Decoder(params_for(w, num_units=9))
+    dec.plan(seq)
+    out1, lse1 = dec.decode(q_nope, q_rope, kv, bt, seq, w.scale)
+    out2, lse2 = dec.decode(q_nope, q_rope, kv, bt, seq, w.scale)
+    torch.cuda.synchronize()
+    assert mla_device_error(clear=True) == 0
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    U, nqb = dec.num_units, w.batch * w.s_q
+    assert dec.sched.cpu().numpy()[8 + 8 * U: 8 + 8 * U + nqb].max() > 1   # some block was split
+    ref_out, ref_lse = oracle_full(w, threads=THREADS)
+    compare(out2.float().cpu().numpy().astype(np.float64), lse2.cpu().numpy().astype(np.float64), ref_out, ref_lse,
+            BF16_TOL, "reused metadata", out_bf16=True)
+
+
 # ------------------------------------------------------------------ FP8 E4M3 latent cache
 
 @pytest.mark.parametrize("num_units", [0, 3])
