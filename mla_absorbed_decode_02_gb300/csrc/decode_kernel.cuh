@@ -509,7 +509,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_QT_FULL));
     };
 
-    // epilogue of a finished piece: O / l -> out (or a split partial), lse
+    // Row-per-thread data (tensor memory's layout) <-> whole-row global accesses go through this
+    // warp's 4 KB of the warpgroup's P / exchange buffer: 32 rows x 128 bytes, 16-byte chunks
+    // XOR-swizzled by row so that both the row-per-lane and the chunk-per-lane passes are
+    // conflict-free.  Callers own the buffer at that point (no P for PV in it, no exchange data
+    // due).
+    const uint32_t stg = my_x + (uint32_t)(warp & 3) * 4096;
+    const int row0 = (warp & 3) * 32;  // this warp's first head row
+    const int sub = lane >> 3, chk = lane & 7;
+    auto stg_row = [&](int row, int c) -> uint32_t { return stg + row * 128 + (((uint32_t)(c ^ (row & 7))) << 4); };
+
+    // absorbed-query half of query block qb -> tensor memory (A operand of the latent score):
+    // 128-byte row segments loaded by 8 lanes each, two 32-column blocks in flight at a time
+    auto load_q_tmem_staged = [&](int qb) {
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(args.q_nope) + (int64_t)qb * H * 256 + 128 * half + 4 * chk;
+      auto fetch = [&](uint4 (&g)[8], int k) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int row = row0 + 4 * i + sub;
+          g[i] = row < H ? *reinterpret_cast<const uint4*>(src + (int64_t)row * 256 + 32 * k) : make_uint4(0, 0, 0, 0);
+        }
+      };
+      auto put = [&](const uint4 (&g)[8], int k) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(stg_row(4 * i + sub, chk)), "r"(g[i].x), "r"(g[i].y),
+                       "r"(g[i].z), "r"(g[i].w)
+                       : "memory");
+        __syncwarp();
+        uint32_t v[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(v[4 * c]), "=r"(v[4 * c + 1]), "=r"(v[4 * c + 2]), "=r"(v[4 * c + 3])
+                       : "r"(stg_row(lane, c))
+                       : "memory");
+        __syncwarp();
+        tmem_st32(tmem + lane_off + TM_Q + 32 * k, v);
+      };
+      uint4 g0[8], g1[8];
+      fetch(g0, 0);
+      fetch(g1, 1);
+      put(g0, 0);
+      fetch(g0, 2);
+      put(g1, 1);
+      fetch(g1, 3);
+      put(g0, 2);
+      put(g1, 3);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_QT_FULL));
+    };
+
+    // epilogue of a finished piece: O / l -> out (or a split partial), lse; whole 128-byte row
+    // segments per 8 lanes through the staging buffer
     int epi_qb = 0, epi_split = 0, epi_piece = -1;
     bool epi_pending = false;
     const uint64_t pol_partial = l2_policy_evict_last();
@@ -517,45 +571,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool split = num_splits[epi_qb] > 1;
       const int slot = split ? split_offset[epi_qb] + epi_split : 0;
       const float inv_l = 1.f / l_tot;
-      const bool write_row = r < H;
+      if (split || args.out_f32) {
+        float* dst = (split ? args.o_acc + (int64_t)slot * H * 512 : reinterpret_cast<float*>(args.out) + (int64_t)epi_qb * H * 512) +
+                     256 * half + 4 * chk;
 #pragma unroll 1
-      for (int c = 0; c < 8; c += 2) {
-        uint32_t v[2][32];
-        tmem_ld32(tmem + lane_off + TM_O + 32 * c, v[0]);
-        tmem_ld32(tmem + lane_off + TM_O + 32 * c + 32, v[1]);
-        tmem_wait_ld();
-        if (write_row) {
+        for (int c = 0; c < 8; ++c) {  // 32 columns per round
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + TM_O + 32 * c, v);
+          tmem_wait_ld();
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int d0 = 256 * half + 32 * (c + h2);
-            if (split || args.out_f32) {
-              float* dst = split ? args.o_acc + ((int64_t)slot * H + r) * 512 + d0
-                                 : reinterpret_cast<float*>(args.out) + ((int64_t)epi_qb * H + r) * 512 + d0;
+          for (int q = 0; q < 8; ++q)
+            asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(stg_row(lane, q)),
+                         "f"(__uint_as_float(v[4 * q]) * inv_l), "f"(__uint_as_float(v[4 * q + 1]) * inv_l),
+                         "f"(__uint_as_float(v[4 * q + 2]) * inv_l), "f"(__uint_as_float(v[4 * q + 3]) * inv_l)
+                         : "memory");
+          __syncwarp();
 #pragma unroll
-              for (int j = 0; j < 32; j += 4) {
-                const float4 o4 = make_float4(__uint_as_float(v[h2][j]) * inv_l, __uint_as_float(v[h2][j + 1]) * inv_l,
-                                              __uint_as_float(v[h2][j + 2]) * inv_l, __uint_as_float(v[h2][j + 3]) * inv_l);
-                if (split)  // read back by the combine right after this kernel: keep it in L2
-                  st_global_v4_hint(dst + j, o4, pol_partial);
-                else
-                  *reinterpret_cast<float4*>(dst + j) = o4;
-              }
-            } else {
-              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.out) + ((int64_t)epi_qb * H + r) * 512 + d0;
-#pragma unroll
-              for (int j = 0; j < 32; j += 8) {
-                uint4 o;
-                o.x = pack_bf16(__uint_as_float(v[h2][j]) * inv_l, __uint_as_float(v[h2][j + 1]) * inv_l);
-                o.y = pack_bf16(__uint_as_float(v[h2][j + 2]) * inv_l, __uint_as_float(v[h2][j + 3]) * inv_l);
-                o.z = pack_bf16(__uint_as_float(v[h2][j + 4]) * inv_l, __uint_as_float(v[h2][j + 5]) * inv_l);
-                o.w = pack_bf16(__uint_as_float(v[h2][j + 6]) * inv_l, __uint_as_float(v[h2][j + 7]) * inv_l);
-                *reinterpret_cast<uint4*>(dst + j) = o;
-              }
+          for (int i = 0; i < 8; ++i) {
+            const int row = 4 * i + sub;
+            float4 o4;
+            asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                         : "=f"(o4.x), "=f"(o4.y), "=f"(o4.z), "=f"(o4.w)
+                         : "r"(stg_row(row, chk))
+                         : "memory");
+            if (row0 + row < H) {
+              float* d = dst + (int64_t)(row0 + row) * 512 + 32 * c;
+              if (split)  // read back by the combine right after this kernel: keep it in L2
+                st_global_v4_hint(d, o4, pol_partial);
+              else
+                *reinterpret_cast<float4*>(d) = o4;
             }
           }
+          __syncwarp();
+        }
+      } else {
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.out) + (int64_t)epi_qb * H * 512 + 256 * half + 8 * chk;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {  // 64 columns per round
+          uint32_t v[2][32];
+          tmem_ld32(tmem + lane_off + TM_O + 64 * c, v[0]);
+          tmem_ld32(tmem + lane_off + TM_O + 64 * c + 32, v[1]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t* u = &v[q >> 2][(q & 3) * 8];
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(stg_row(lane, q)),
+                         "r"(pack_bf16(__uint_as_float(u[0]) * inv_l, __uint_as_float(u[1]) * inv_l)),
+                         "r"(pack_bf16(__uint_as_float(u[2]) * inv_l, __uint_as_float(u[3]) * inv_l)),
+                         "r"(pack_bf16(__uint_as_float(u[4]) * inv_l, __uint_as_float(u[5]) * inv_l)),
+                         "r"(pack_bf16(__uint_as_float(u[6]) * inv_l, __uint_as_float(u[7]) * inv_l))
+                         : "memory");
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int row = 4 * i + sub;
+            uint4 o;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(o.x), "=r"(o.y), "=r"(o.z), "=r"(o.w)
+                         : "r"(stg_row(row, chk))
+                         : "memory");
+            if (row0 + row < H) *reinterpret_cast<uint4*>(dst + (int64_t)(row0 + row) * 512 + 64 * c) = o;
+          }
+          __syncwarp();
         }
       }
-      if (write_row && half == 0) {
+      if (r < H && half == 0) {
         const float lse = (m_fin + log2f(l_tot)) * 0.69314718055994530942f;
         if (split)
           args.lse_acc[(int64_t)slot * H + r] = lse;
@@ -613,8 +694,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---- own partial scores; the score buffer is free again right after the read
         if (!(ok = wait_warp(bar(B_S_FULL + sb), ph, wc, kSiteSFull))) break;
         tc_fence_after();
-        // QK(t) is done: if it was the piece's last, the query half in tensor memory is free
-        if (x.last && has_np) load_q_tmem(np.qb);
+        // QK(t) is done: if it was the piece's last, the query half in tensor memory is free.  From
+        // tile 2 on, this warpgroup's buffer (P(t-2), read by PV(t-2)) is not handed back for X(t)
+        // yet: the load is staged in it.  Before that the buffer may already be receiving.
+        bool handed_back = false;
+        if (__builtin_expect(x.last && has_np, 0)) {
+          if (t < 2) {
+            load_q_tmem(np.qb);
+          } else {
+            if (!(ok = wait_warp(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) break;
+            load_q_tmem_staged(np.qb);
+            if (lane == 0) mbar_arrive_remote(peer_bar0 + 8 * (B_X_FREE + sb));
+            handed_back = true;
+          }
+        }
         uint64_t sc[32];  // score pairs: columns (2u, 2u + 1) in pair u
         float beta = 0.f;  // bias the block-float decode leaves on every score of the row
         {
@@ -633,7 +726,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         // this warpgroup's buffer held P(t-2): hand it back to the peer once PV(t-2) is done
         // (a relaxed arrive, made to depend on the values read from the buffer)
-        if (t >= 2) {
+        if (t >= 2 && !handed_back) {
           if (!(ok = wait_warp(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) break;
           if (lane == 0) mbar_arrive_remote_relaxed(peer_bar0 + 8 * (B_X_FREE + sb), slot_dep);
         }
@@ -747,6 +840,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(B_ML + sb));
         // ---- O is touched only after PV(t-1): the previous piece's epilogue, a rescale
         const bool any_rescale = __any_sync(0xffffffffu, alpha != 1.f);
+        // every thread of the warpgroup has read its rows of the exchange data: from here the
+        // buffer takes the epilogue's staging and then P(t)
+        asm volatile("bar.sync %0, 128;" ::"r"(1 + w) : "memory");
         if (epi_pending || any_rescale) {
           if (!(ok = wait_warp(bar(B_P_FREE + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSitePEmpty))) break;
           tc_fence_after();
@@ -767,9 +863,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_wait_st();
           }
         }
-        // ---- publish P over the decoded exchange data (PV(t-2) was waited for above); every
-        // thread of the warpgroup has read its rows of the exchange data before any P row lands
-        asm volatile("bar.sync %0, 128;" ::"r"(1 + w) : "memory");
+        // ---- publish P over the decoded exchange data (PV(t-2) was waited for above)
         if (valid < kTileTok) {
           // rows past the sequence end must not reach the PV product (0 * garbage): zero them
           const uint32_t sbase = base + (t % kStages) * kStageBytes;
