@@ -374,7 +374,7 @@ def run_ours(args, w, peaks, world, rank, local):
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "peak_source": f"{peaks['source']} (cuBLAS bf16, burst)"}
     roof["traffic"] = committed_traffic(args.workload)
-    roof["kernel"] = "mla_decode_bf16_kernel"
+    roof["kernel"] = "mla_decode_fp8_kernel" if w.kv_dtype == "fp8" else "mla_decode_bf16_kernel"
     roof["kernel_ms"] = t_dec * 1e3
     res = {
         "metric": METRIC, "value": value, "unit": "% of GB300 roofline (summed over GPUs)", "n_gpus": n,

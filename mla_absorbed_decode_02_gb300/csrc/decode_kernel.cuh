@@ -294,8 +294,10 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_bf16_kernel(const __grid_constant__ DecodeArgs args) {
+// The kernel body, instantiated once per cache format (no code of the other format in the
+// instruction stream of either).
+template <bool kFp8>
+__device__ __forceinline__ void decode_body(const DecodeArgs& args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t base = smem_addr(smem);
@@ -374,7 +376,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&args.map_qr);
       prefetch_tensormap(&args.map_kvc);
       prefetch_tensormap(&args.map_kvr);
-      if (args.kv_fp8) prefetch_tensormap(&args.map_kvs);
+      if (kFp8) prefetch_tensormap(&args.map_kvs);
       const uint64_t pol_kv = l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
       TileCursor cur;
@@ -393,7 +395,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int b = ti.qb / args.s_q;
         const int page = args.block_table[(int64_t)b * args.max_pages + ti.tile];
         const uint32_t sbase = base + st * kStageBytes;
-        if (args.kv_fp8) {  // 656-byte rows: codes of this half, its RoPE half, the 4 tile scales
+        if (kFp8) {  // 656-byte rows: codes of this half, its RoPE half, the 4 tile scales
           mbar_arrive_expect_tx(bar(B_KV_FULL + st), kFp8StageTx);
           tma_load_2d(sbase + kStageCodes, &args.map_kvc, bar(B_KV_FULL + st), 256 * half, page * 64, pol_kv);
           tma_load_2d(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 528 + 64 * half, page * 64, pol_kv);
@@ -428,7 +430,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ++piece_no;
           }
           const uint32_t st = t % kStages, sb = t & 1;
-          if (!wait_one(bar((args.kv_fp8 ? B_K_READY : B_KV_FULL) + st), (t / kStages) & 1, wc, kSiteKvFull)) break;
+          if (!wait_one(bar((kFp8 ? B_K_READY : B_KV_FULL) + st), (t / kStages) & 1, wc, kSiteKvFull)) break;
           if (!wait_one(bar(B_S_EMPTY + sb), ((t >> 1) & 1) ^ 1, wc, kSiteSEmpty)) break;
           tc_fence_after();
           const uint32_t sbase = base + st * kStageBytes;
@@ -671,7 +673,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_K_READY + st));
       return true;
     };
-    if (args.kv_fp8 && w < n_tiles) ok = expand_tile(w);
+    if (kFp8 && w < n_tiles) ok = expand_tile(w);
     TileCursor cursor;
     cursor.init(walker0);
     TileInfo x;
@@ -883,7 +885,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_P_FULL + sb));
-        if (args.kv_fp8 && t + 2 < n_tiles && !(ok = expand_tile(t + 2))) break;
+        if (kFp8 && t + 2 < n_tiles && !(ok = expand_tile(t + 2))) break;
       }
       if (x.last) {  // the warpgroup of the next tile finishes this piece
         epi_qb = x.qb;
@@ -915,6 +917,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_decode_bf16_kernel(const __grid_constant__ DecodeArgs args) {
+  decode_body<false>(args);
+}
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_decode_fp8_kernel(const __grid_constant__ DecodeArgs args) {
+  decode_body<true>(args);
 }
 
 }  // namespace mla

@@ -167,7 +167,9 @@ int32_t device_info(DeviceInfo** out) {
   if (!d.ready) {
     if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
     if (cudaFuncSetAttribute(mla_decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-        cudaSuccess)
+            cudaSuccess ||
+        cudaFuncSetAttribute(mla_decode_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+            cudaSuccess)
       return MLA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (d.sm_count / 2), 1, 1);
@@ -373,7 +375,9 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cfg.numAttrs = 0;  // cluster shape comes from __cluster_dims__
-  return cudaLaunchKernelEx(&cfg, mla_decode_bf16_kernel, a) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  const cudaError_t e = a.kv_fp8 ? cudaLaunchKernelEx(&cfg, mla_decode_fp8_kernel, a)
+                                 : cudaLaunchKernelEx(&cfg, mla_decode_bf16_kernel, a);
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 int32_t mla_combine(const mla_decode_params* p, void* out, float* lse, const void* sched, void* workspace,
