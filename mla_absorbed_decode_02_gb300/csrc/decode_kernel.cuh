@@ -43,6 +43,8 @@
 // = tensor-memory allocator, warp 3 = PV issuer, warps 4..7 / 8..11 = softmax
 // warpgroups 0 / 1.
 #pragma once
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace mla {
@@ -679,6 +681,209 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
     TileInfo x;
     uint32_t t = 0;
     int piece = -1;
+    // One tile of this warpgroup.  Two instances: the full one for the first and the last tile
+    // of a piece (query load for the next piece, the finished piece's epilogue, a partial last
+    // page), and a lean one for the tiles in between, which carries none of that code -- the
+    // per-tile loop is sensitive to the size of its instruction stream.  (A partial page is
+    // always a piece's last tile; the epilogue is always due at a piece's first.)
+    auto tile = [&](auto full) -> bool {
+      constexpr bool kFull = decltype(full)::value;
+          const uint32_t sb = w, ph = (t >> 1) & 1;
+          // ---- own partial scores; the score buffer is free again right after the read
+          if (!(ok = wait_warp(bar(B_S_FULL + sb), ph, wc, kSiteSFull))) return false;
+          tc_fence_after();
+          // QK(t) is done: if it was the piece's last, the query half in tensor memory is free.  From
+          // tile 2 on, this warpgroup's buffer (P(t-2), read by PV(t-2)) is not handed back for X(t)
+          // yet: the load is staged in it.  Before that the buffer may already be receiving.
+          bool handed_back = false;
+          if (kFull && x.last && has_np) {
+            if (t < 2) {
+              load_q_tmem(np.qb);
+            } else {
+              if (!(ok = wait_warp(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) return false;
+              load_q_tmem_staged(np.qb);
+              if (lane == 0) mbar_arrive_remote(peer_bar0 + 8 * (B_X_FREE + sb));
+              handed_back = true;
+            }
+          }
+          uint64_t sc[32];  // score pairs: columns (2u, 2u + 1) in pair u
+          float beta = 0.f;  // bias the block-float decode leaves on every score of the row
+          {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tmem + lane_off + TM_S + 64 * sb, v0);
+            tmem_ld32(tmem + lane_off + TM_S + 64 * sb + 32, v1);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_S_EMPTY + sb));
+  #pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              sc[u] = pack_b32x2(v0[2 * u], v0[2 * u + 1]);
+              sc[16 + u] = pack_b32x2(v1[2 * u], v1[2 * u + 1]);
+            }
+          }
+          // this warpgroup's buffer held P(t-2): hand it back to the peer once PV(t-2) is done
+          // (a relaxed arrive, made to depend on the values read from the buffer)
+          if (t >= 2 && !handed_back) {
+            if (!(ok = wait_warp(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) return false;
+            if (lane == 0) mbar_arrive_remote_relaxed(peer_bar0 + 8 * (B_X_FREE + sb), slot_dep);
+          }
+          const int valid = x.valid;
+          if (kFull && valid < kTileTok) mask_pairs(sc, valid, 0.f);  // columns past the sequence end: sent as 0
+          // ---- encode (16-bit block floating point, one exponent per 32 columns) and send
+          {
+            float a[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+            for (int u = 0; u < 32; ++u) {
+              float x0, x1;
+              unpack_f32x2(sc[u], x0, x1);
+              a[(2 * u) & 3] = fmaxf(a[(2 * u) & 3], fabsf(x0));
+              a[(2 * u + 1) & 3] = fmaxf(a[(2 * u + 1) & 3], fabsf(x1));
+            }
+            const int e = bfp_exponent(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])));
+            const uint64_t k = splat_f32x2(pow2f(14 - e));
+            uint32_t pk[32];
+  #pragma unroll
+            for (int u = 0; u < 32; ++u) pk[u] = bfp_pack_pair(sc[u], k);
+            if (!(ok = wait_warp(bar(B_X_FREE + sb), ph ^ 1, wc, kSiteXFree))) return false;
+            const uint32_t full = peer_bar0 + 8 * (B_X_FULL + sb);
+  #pragma unroll
+            for (int j = 0; j < 8; ++j)
+              st_async_v4(peer_x + (j * kRows + r) * 16, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3], full);
+            st_async_b32(peer_xe + r * 4, (uint32_t)e, full);
+          }
+          // ---- the peer's half of the same scores
+          if ((warp & 3) == 0 && lane == 0) mbar_arrive_expect_tx(bar(B_X_FULL + sb), kXBytes);
+          if (!(ok = wait_warp<true>(bar(B_X_FULL + sb), ph, wc, kSiteXFull))) return false;
+          {
+            uint32_t pe;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pe) : "r"(my_xe + r * 4));
+            slot_dep = pe;
+            const float kpf = pow2f((int)pe - 14);
+            const uint64_t kp = splat_f32x2(kpf);
+            beta = kBfpBias * kpf;  // exact: a power of two times a 24-bit integer
+  #pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint32_t wv[4];
+              asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                           : "=r"(wv[0]), "=r"(wv[1]), "=r"(wv[2]), "=r"(wv[3])
+                           : "r"(my_x + (j * kRows + r) * 16));
+              slot_dep ^= wv[0] ^ wv[3];
+  #pragma unroll
+              for (int q = 0; q < 4; ++q) sc[4 * j + q] = ffma_f32x2(bfp_unpack_pair(wv[q]), kp, sc[4 * j + q]);
+            }
+          }
+          if (kFull && valid < kTileTok) mask_pairs(sc, valid, -INFINITY);
+          float cm;
+          {
+            float c[4];
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float x0, x1;
+              unpack_f32x2(sc[q], x0, x1);
+              c[q] = fmaxf(x0, x1);
+            }
+  #pragma unroll
+            for (int u = 4; u < 32; ++u) {
+              float x0, x1;
+              unpack_f32x2(sc[u], x0, x1);
+              c[u & 3] = fmax3(c[u & 3], x0, x1);
+            }
+            cm = (fmax3(c[0], c[1], fmaxf(c[2], c[3])) - beta) * sl2;  // log2 units (sl2 > 0)
+          }
+          // ---- running max: decided from the previous tile's (the other warpgroup's)
+          float m_prev = 0.f, l_other = 0.f;
+          if (t > 0) {
+            if (!(ok = wait_warp(bar(B_ML + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSiteML))) return false;
+            m_prev = ml[((sb ^ 1) * 2) * kRows + r];
+            l_other = ml[((sb ^ 1) * 2 + 1) * kRows + r];
+          }
+          float m = m_prev, alpha = 1.f;
+          if (kFull && x.first) {
+            m = cm;  // finite: token 0 of a piece's first tile is visible
+          } else if (cm > m_prev + 8.f) {
+            m = cm;
+            alpha = exp2f(m_prev - cm);
+          }
+          // the finished piece (last tile t-1) takes both warpgroups' row sums at its final max
+          float epi_l = 0.f;
+          if (kFull && epi_pending) epi_l = l_other + (my_piece == epi_piece ? l_mine * exp2f(m_ref - m_prev) : 0.f);
+          uint32_t pp[32];
+          float rsum;
+          {
+            const uint64_t s2 = splat_f32x2(sl2), nm = splat_f32x2(-fmaf(beta, sl2, m));
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+  #pragma unroll
+            for (int u = 0; u < 32; ++u) {
+              float x0, x1;
+              unpack_f32x2(ffma_f32x2(sc[u], s2, nm), x0, x1);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              pp[u] = pack_bf16(p0, p1);
+              acc[u & 3] = fadd_f32x2(acc[u & 3], pack_f32x2(p0, p1));
+            }
+            float z[8];
+            unpack_f32x2(fadd_f32x2(fadd_f32x2(acc[0], acc[1]), fadd_f32x2(acc[2], acc[3])), z[0], z[1]);
+            rsum = z[0] + z[1];
+          }
+          if (piece != my_piece) {
+            my_piece = piece;
+            l_mine = 0.f;
+            m_ref = m;
+          }
+          l_mine = l_mine * exp2f(m_ref - m) + rsum;
+          m_ref = m;
+          ml[(sb * 2) * kRows + r] = m;
+          ml[(sb * 2 + 1) * kRows + r] = l_mine;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_ML + sb));
+          // ---- O is touched only after PV(t-1): the previous piece's epilogue, a rescale
+          const bool any_rescale = __any_sync(0xffffffffu, alpha != 1.f);
+          // every thread of the warpgroup has read its rows of the exchange data: from here the
+          // buffer takes the epilogue's staging and then P(t)
+          asm volatile("bar.sync %0, 128;" ::"r"(1 + w) : "memory");
+          if ((kFull && epi_pending) || any_rescale) {
+            if (!(ok = wait_warp(bar(B_P_FREE + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSitePEmpty))) return false;
+            tc_fence_after();
+            if (kFull && epi_pending) {
+              epilogue(m_prev, epi_l);
+              epi_pending = false;
+            }
+            if (any_rescale) {
+  #pragma unroll 1
+              for (int c = 0; c < 8; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + TM_O + 32 * c, v);
+                tmem_wait_ld();
+  #pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+                tmem_st32(tmem + lane_off + TM_O + 32 * c, v);
+              }
+              tmem_wait_st();
+            }
+          }
+          // ---- publish P over the decoded exchange data (PV(t-2) was waited for above)
+          if (kFull && valid < kTileTok) {
+            // rows past the sequence end must not reach the PV product (0 * garbage): zero them
+            const uint32_t sbase = base + (t % kStages) * kStageBytes;
+            const int nz = (kTileTok - valid) * 4 * 8;  // 16-byte chunks: rows x 4 blocks x 8
+            for (int idx = r; idx < nz; idx += kRows) {
+              const int row = valid + idx / 32, blk = (idx / 8) & 3, ch = idx & 7;
+              asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(sbase + blk * kLatBlock + row * 128 + ch * 16),
+                           "r"(0u));
+            }
+          }
+          const uint32_t prow = base + SM_P + sb * kPBytes + r * 128;
+  #pragma unroll
+          for (int ch = 0; ch < 8; ++ch)  // P row: K-major, 128-byte swizzle
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((((uint32_t)ch) ^ (r & 7)) << 4)),
+                         "r"(pp[4 * ch]), "r"(pp[4 * ch + 1]), "r"(pp[4 * ch + 2]), "r"(pp[4 * ch + 3]));
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_P_FULL + sb));
+          if (kFp8 && t + 2 < n_tiles && !(ok = expand_tile(t + 2))) return false;
+      return true;
+    };
     while (ok && cursor.next(x)) {
       if (x.first) {
         ++piece;
@@ -692,200 +897,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
         }
       }
       if ((t & 1) == w) {
-        const uint32_t sb = w, ph = (t >> 1) & 1;
-        // ---- own partial scores; the score buffer is free again right after the read
-        if (!(ok = wait_warp(bar(B_S_FULL + sb), ph, wc, kSiteSFull))) break;
-        tc_fence_after();
-        // QK(t) is done: if it was the piece's last, the query half in tensor memory is free.  From
-        // tile 2 on, this warpgroup's buffer (P(t-2), read by PV(t-2)) is not handed back for X(t)
-        // yet: the load is staged in it.  Before that the buffer may already be receiving.
-        bool handed_back = false;
-        if (__builtin_expect(x.last && has_np, 0)) {
-          if (t < 2) {
-            load_q_tmem(np.qb);
-          } else {
-            if (!(ok = wait_warp(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) break;
-            load_q_tmem_staged(np.qb);
-            if (lane == 0) mbar_arrive_remote(peer_bar0 + 8 * (B_X_FREE + sb));
-            handed_back = true;
-          }
+        if (!(x.first || x.last ? tile(std::true_type{}) : tile(std::false_type{}))) {
+          ok = false;
+          break;
         }
-        uint64_t sc[32];  // score pairs: columns (2u, 2u + 1) in pair u
-        float beta = 0.f;  // bias the block-float decode leaves on every score of the row
-        {
-          uint32_t v0[32], v1[32];
-          tmem_ld32(tmem + lane_off + TM_S + 64 * sb, v0);
-          tmem_ld32(tmem + lane_off + TM_S + 64 * sb + 32, v1);
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_S_EMPTY + sb));
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            sc[u] = pack_b32x2(v0[2 * u], v0[2 * u + 1]);
-            sc[16 + u] = pack_b32x2(v1[2 * u], v1[2 * u + 1]);
-          }
-        }
-        // this warpgroup's buffer held P(t-2): hand it back to the peer once PV(t-2) is done
-        // (a relaxed arrive, made to depend on the values read from the buffer)
-        if (t >= 2 && !handed_back) {
-          if (!(ok = wait_warp(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) break;
-          if (lane == 0) mbar_arrive_remote_relaxed(peer_bar0 + 8 * (B_X_FREE + sb), slot_dep);
-        }
-        const int valid = x.valid;
-        if (valid < kTileTok) mask_pairs(sc, valid, 0.f);  // columns past the sequence end: sent as 0
-        // ---- encode (16-bit block floating point, one exponent per 32 columns) and send
-        {
-          float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            float x0, x1;
-            unpack_f32x2(sc[u], x0, x1);
-            a[(2 * u) & 3] = fmaxf(a[(2 * u) & 3], fabsf(x0));
-            a[(2 * u + 1) & 3] = fmaxf(a[(2 * u + 1) & 3], fabsf(x1));
-          }
-          const int e = bfp_exponent(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])));
-          const uint64_t k = splat_f32x2(pow2f(14 - e));
-          uint32_t pk[32];
-#pragma unroll
-          for (int u = 0; u < 32; ++u) pk[u] = bfp_pack_pair(sc[u], k);
-          if (!(ok = wait_warp(bar(B_X_FREE + sb), ph ^ 1, wc, kSiteXFree))) break;
-          const uint32_t full = peer_bar0 + 8 * (B_X_FULL + sb);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_async_v4(peer_x + (j * kRows + r) * 16, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3], full);
-          st_async_b32(peer_xe + r * 4, (uint32_t)e, full);
-        }
-        // ---- the peer's half of the same scores
-        if ((warp & 3) == 0 && lane == 0) mbar_arrive_expect_tx(bar(B_X_FULL + sb), kXBytes);
-        if (!(ok = wait_warp<true>(bar(B_X_FULL + sb), ph, wc, kSiteXFull))) break;
-        {
-          uint32_t pe;
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pe) : "r"(my_xe + r * 4));
-          slot_dep = pe;
-          const float kpf = pow2f((int)pe - 14);
-          const uint64_t kp = splat_f32x2(kpf);
-          beta = kBfpBias * kpf;  // exact: a power of two times a 24-bit integer
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint32_t wv[4];
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(wv[0]), "=r"(wv[1]), "=r"(wv[2]), "=r"(wv[3])
-                         : "r"(my_x + (j * kRows + r) * 16));
-            slot_dep ^= wv[0] ^ wv[3];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) sc[4 * j + q] = ffma_f32x2(bfp_unpack_pair(wv[q]), kp, sc[4 * j + q]);
-          }
-        }
-        if (valid < kTileTok) mask_pairs(sc, valid, -INFINITY);
-        float cm;
-        {
-          float c[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float x0, x1;
-            unpack_f32x2(sc[q], x0, x1);
-            c[q] = fmaxf(x0, x1);
-          }
-#pragma unroll
-          for (int u = 4; u < 32; ++u) {
-            float x0, x1;
-            unpack_f32x2(sc[u], x0, x1);
-            c[u & 3] = fmax3(c[u & 3], x0, x1);
-          }
-          cm = (fmax3(c[0], c[1], fmaxf(c[2], c[3])) - beta) * sl2;  // log2 units (sl2 > 0)
-        }
-        // ---- running max: decided from the previous tile's (the other warpgroup's)
-        float m_prev = 0.f, l_other = 0.f;
-        if (t > 0) {
-          if (!(ok = wait_warp(bar(B_ML + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSiteML))) break;
-          m_prev = ml[((sb ^ 1) * 2) * kRows + r];
-          l_other = ml[((sb ^ 1) * 2 + 1) * kRows + r];
-        }
-        float m = m_prev, alpha = 1.f;
-        if (x.first) {
-          m = cm;  // finite: token 0 of a piece's first tile is visible
-        } else if (cm > m_prev + 8.f) {
-          m = cm;
-          alpha = exp2f(m_prev - cm);
-        }
-        // the finished piece (last tile t-1) takes both warpgroups' row sums at its final max
-        float epi_l = 0.f;
-        if (epi_pending) epi_l = l_other + (my_piece == epi_piece ? l_mine * exp2f(m_ref - m_prev) : 0.f);
-        uint32_t pp[32];
-        float rsum;
-        {
-          const uint64_t s2 = splat_f32x2(sl2), nm = splat_f32x2(-fmaf(beta, sl2, m));
-          uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            float x0, x1;
-            unpack_f32x2(ffma_f32x2(sc[u], s2, nm), x0, x1);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            pp[u] = pack_bf16(p0, p1);
-            acc[u & 3] = fadd_f32x2(acc[u & 3], pack_f32x2(p0, p1));
-          }
-          float z[8];
-          unpack_f32x2(fadd_f32x2(fadd_f32x2(acc[0], acc[1]), fadd_f32x2(acc[2], acc[3])), z[0], z[1]);
-          rsum = z[0] + z[1];
-        }
-        if (piece != my_piece) {
-          my_piece = piece;
-          l_mine = 0.f;
-          m_ref = m;
-        }
-        l_mine = l_mine * exp2f(m_ref - m) + rsum;
-        m_ref = m;
-        ml[(sb * 2) * kRows + r] = m;
-        ml[(sb * 2 + 1) * kRows + r] = l_mine;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_ML + sb));
-        // ---- O is touched only after PV(t-1): the previous piece's epilogue, a rescale
-        const bool any_rescale = __any_sync(0xffffffffu, alpha != 1.f);
-        // every thread of the warpgroup has read its rows of the exchange data: from here the
-        // buffer takes the epilogue's staging and then P(t)
-        asm volatile("bar.sync %0, 128;" ::"r"(1 + w) : "memory");
-        if (epi_pending || any_rescale) {
-          if (!(ok = wait_warp(bar(B_P_FREE + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSitePEmpty))) break;
-          tc_fence_after();
-          if (epi_pending) {
-            epilogue(m_prev, epi_l);
-            epi_pending = false;
-          }
-          if (any_rescale) {
-#pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-              uint32_t v[32];
-              tmem_ld32(tmem + lane_off + TM_O + 32 * c, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-              tmem_st32(tmem + lane_off + TM_O + 32 * c, v);
-            }
-            tmem_wait_st();
-          }
-        }
-        // ---- publish P over the decoded exchange data (PV(t-2) was waited for above)
-        if (valid < kTileTok) {
-          // rows past the sequence end must not reach the PV product (0 * garbage): zero them
-          const uint32_t sbase = base + (t % kStages) * kStageBytes;
-          const int nz = (kTileTok - valid) * 4 * 8;  // 16-byte chunks: rows x 4 blocks x 8
-          for (int idx = r; idx < nz; idx += kRows) {
-            const int row = valid + idx / 32, blk = (idx / 8) & 3, ch = idx & 7;
-            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(sbase + blk * kLatBlock + row * 128 + ch * 16),
-                         "r"(0u));
-          }
-        }
-        const uint32_t prow = base + SM_P + sb * kPBytes + r * 128;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)  // P row: K-major, 128-byte swizzle
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((((uint32_t)ch) ^ (r & 7)) << 4)),
-                       "r"(pp[4 * ch]), "r"(pp[4 * ch + 1]), "r"(pp[4 * ch + 2]), "r"(pp[4 * ch + 3]));
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_P_FULL + sb));
-        if (kFp8 && t + 2 < n_tiles && !(ok = expand_tile(t + 2))) break;
       }
       if (x.last) {  // the warpgroup of the next tile finishes this piece
         epi_qb = x.qb;
