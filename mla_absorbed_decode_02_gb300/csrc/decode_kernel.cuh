@@ -351,6 +351,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
     tmem_relinquish();
   }
   tc_fence_before();
+  __syncwarp();  // (warp 0 ran the set-up on one lane: the CTA and cluster barriers below take whole warps)
   __syncthreads();
   cluster_sync();  // peer barriers initialised before any remote arrive / st.async
   tc_fence_after();
@@ -925,6 +926,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
   }
 
   // ---------------------------------------------------------------- teardown
+  __syncwarp();  // the producer and MMA-issuer warps worked on one lane: reconverge before the barriers
   __syncthreads();
   if (*abort_flag) drain_delay(200000);  // in-flight TMA / st.async / MMA land before release
   cluster_sync();                        // the peer no longer touches our shared memory

@@ -40,44 +40,70 @@ __global__ void __launch_bounds__(1024) mla_sched_kernel(const int32_t* seqlens,
 // out = sum_i exp(lse_i - lse) * out_i, lse = M + ln sum_i exp(lse_i - M), M = max_i lse_i
 // (the merge of split-KV partial results, "MLA inference: two computation paths and
 // FlashMLA", section "Decode attention becomes a compute problem").  Query blocks that see
-// no key get out = 0, lse = -inf.  One CTA of 128 threads per (query block, head).
-__global__ void __launch_bounds__(128) mla_combine_kernel(const int32_t* sched, int U, int NQB, int H,
+// no key get out = 0, lse = -inf.  One CTA of 256 threads per (query block, 16 heads): the
+// 16 combined LSEs first (two heads per warp, the splits spread over 16 lanes), then every
+// thread streams 8 float4 columns of one head per split, each split's 8 loads in flight together.
+constexpr int kCombineHeads = 16;
+__global__ void __launch_bounds__(256) mla_combine_kernel(const int32_t* sched, int U, int NQB, int H,
                                                           const float* o_acc, const float* lse_acc, void* out,
                                                           float* lse, int out_f32) {
   pdl_wait_prerequisites();  // the decode kernel before it in the stream has finished
-  const int qb = blockIdx.x, h = blockIdx.y, d = threadIdx.x * 4;
+  const int qb = blockIdx.x, h0 = blockIdx.y * kCombineHeads;
   const int32_t* num_splits = sched + kSchedHeader + kUnitInts * U;
   const int32_t* split_offset = num_splits + NQB;
   const int ns = num_splits[qb];
-  if (ns == 1) return;
-  const int64_t row = (int64_t)qb * H + h;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float L = -INFINITY;
-  if (ns > 1) {
-    const int off = split_offset[qb];
+  if (ns == 1) return;  // the decode kernel wrote this query block's output itself
+  const int off = ns > 1 ? split_offset[qb] : 0;
+  __shared__ float s_lse[kCombineHeads];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {
+    const int hh = 2 * warp + (lane >> 4), h = h0 + hh, sub = lane & 15;
     float M = -INFINITY;
-    for (int i = 0; i < ns; ++i) M = fmaxf(M, lse_acc[(int64_t)(off + i) * H + h]);
+    for (int i = sub; i < ns && h < H; i += 16) M = fmaxf(M, lse_acc[(int64_t)(off + i) * H + h]);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float S = 0.f;
-    for (int i = 0; i < ns; ++i) S += expf(lse_acc[(int64_t)(off + i) * H + h] - M);
-    L = M + logf(S);
-    for (int i = 0; i < ns; ++i) {
-      const float wgt = expf(lse_acc[(int64_t)(off + i) * H + h] - L);
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(o_acc + ((int64_t)(off + i) * H + h) * 512 + d));
-      acc[0] += wgt * v.x;
-      acc[1] += wgt * v.y;
-      acc[2] += wgt * v.z;
-      acc[3] += wgt * v.w;
+    if (M > -INFINITY)
+      for (int i = sub; i < ns && h < H; i += 16) S += expf(lse_acc[(int64_t)(off + i) * H + h] - M);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+    if (sub == 0) s_lse[hh] = M > -INFINITY ? M + logf(S) : -INFINITY;
+  }
+  __syncthreads();
+  const int hh = tid >> 4, h = h0 + hh, c = tid & 15;  // columns 4 (c + 16 k), k < 8
+  if (h >= H) return;
+  const float L = s_lse[hh];
+  float4 acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = 0; i < ns; ++i) {
+    const float wgt = expf(lse_acc[(int64_t)(off + i) * H + h] - L);
+    const float4* src = reinterpret_cast<const float4*>(o_acc + ((int64_t)(off + i) * H + h) * 512) + c;
+    float4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = __ldcs(src + 16 * k);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      acc[k].x += wgt * v[k].x;
+      acc[k].y += wgt * v[k].y;
+      acc[k].z += wgt * v[k].z;
+      acc[k].w += wgt * v[k].w;
     }
   }
-  if (out_f32) {
-    *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + row * 512 + d) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  } else {
-    uint2 o;
-    o.x = pack_bf16(acc[0], acc[1]);
-    o.y = pack_bf16(acc[2], acc[3]);
-    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + row * 512 + d) = o;
+  const int64_t row = (int64_t)qb * H + h;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int d = 4 * (c + 16 * k);
+    if (out_f32) {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + row * 512 + d) = acc[k];
+    } else {
+      uint2 o;
+      o.x = pack_bf16(acc[k].x, acc[k].y);
+      o.y = pack_bf16(acc[k].z, acc[k].w);
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + row * 512 + d) = o;
+    }
   }
-  if (threadIdx.x == 0) lse[row] = L;
+  if (c == 0) lse[row] = L;
 }
 
 // ----------------------------------------------------------------- FP8 cache writer
@@ -397,8 +423,8 @@ int32_t mla_combine(const mla_decode_params* p, void* out, float* lse, const voi
   // programmatic dependent launch: this grid is set up while the decode kernel before it
   // drains, and waits (griddepcontrol.wait) for it before reading the partials
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(NQB, H, 1);
-  cfg.blockDim = dim3(128, 1, 1);
+  cfg.gridDim = dim3(NQB, (H + kCombineHeads - 1) / kCombineHeads, 1);
+  cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
