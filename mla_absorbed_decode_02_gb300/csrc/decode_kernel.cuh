@@ -572,7 +572,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
     int epi_qb = 0, epi_split = 0, epi_piece = -1;
     bool epi_pending = false;
     const uint64_t pol_partial = l2_policy_evict_last();
-    auto epilogue = [&](float m_fin, float l_tot) {
+    // (columns: part `part` of `nparts` equal parts of this CTA's 256)
+    auto epilogue = [&](float m_fin, float l_tot, int part, int nparts) {
       const bool split = num_splits[epi_qb] > 1;
       const int slot = split ? split_offset[epi_qb] + epi_split : 0;
       const float inv_l = 1.f / l_tot;
@@ -580,7 +581,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
         float* dst = (split ? args.o_acc + (int64_t)slot * H * 512 : reinterpret_cast<float*>(args.out) + (int64_t)epi_qb * H * 512) +
                      256 * half + 4 * chk;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {  // 32 columns per round
+        for (int c = 8 * part / nparts; c < 8 * (part + 1) / nparts; ++c) {  // 32 columns per round
           uint32_t v[32];
           tmem_ld32(tmem + lane_off + TM_O + 32 * c, v);
           tmem_wait_ld();
@@ -612,7 +613,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
       } else {
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.out) + (int64_t)epi_qb * H * 512 + 256 * half + 8 * chk;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {  // 64 columns per round
+        for (int c = 4 * part / nparts; c < 4 * (part + 1) / nparts; ++c) {  // 64 columns per round
           uint32_t v[2][32];
           tmem_ld32(tmem + lane_off + TM_O + 64 * c, v[0]);
           tmem_ld32(tmem + lane_off + TM_O + 64 * c + 32, v[1]);
@@ -641,7 +642,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           __syncwarp();
         }
       }
-      if (r < H && half == 0) {
+      if (r < H && half == 0 && part == 0) {
         const float lse = (m_fin + log2f(l_tot)) * 0.69314718055994530942f;
         if (split)
           args.lse_acc[(int64_t)slot * H + r] = lse;
@@ -846,7 +847,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
             if (!(ok = wait_warp(bar(B_P_FREE + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSitePEmpty))) return false;
             tc_fence_after();
             if (kFull && epi_pending) {
-              epilogue(m_prev, epi_l);
+              epilogue(m_prev, epi_l, 0, 1);
               epi_pending = false;
             }
             if (any_rescale) {
@@ -911,16 +912,28 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
       }
       ++t;
     }
-    if (ok && epi_pending) {  // the unit's last piece ended with the other warpgroup's tile t-1
+    // The unit's last piece: both warpgroups write half of its columns each, from the same final
+    // max and row sum (same operands, same operations).  The owner of the last tile t-1 takes the
+    // other warpgroup's share from what that one published for tile t-2 (if t-2 is in the piece,
+    // i.e. t-1 did not open it; x still describes tile t-1), the other one from what the owner
+    // published for t-1.
+    if (ok && t > 0) {
       const uint32_t pp = (t - 1) & 1;
-      if (wait_warp(bar(B_ML + pp), ((t - 1) >> 1) & 1, wc, kSiteML)) {
-        const float m_fin = ml[(pp * 2) * kRows + r];
+      const bool owner = pp == w;
+      float m_fin = m_ref, l_tot = 0.f;
+      bool go = true;
+      if (owner) {
+        const uint32_t po = pp ^ 1;
+        l_tot = l_mine + (x.first ? 0.f : ml[(po * 2 + 1) * kRows + r] * exp2f(ml[(po * 2) * kRows + r] - m_fin));
+      } else {  // epi_pending: the other warpgroup's tile t-1 ended the piece
+        go = wait_warp(bar(B_ML + pp), ((t - 1) >> 1) & 1, wc, kSiteML);
+        m_fin = ml[(pp * 2) * kRows + r];
         const float l_other = ml[(pp * 2 + 1) * kRows + r];
-        const float l_tot = l_other + (my_piece == epi_piece ? l_mine * exp2f(m_ref - m_fin) : 0.f);
-        if (wait_warp(bar(B_P_FREE + pp), ((t - 1) >> 1) & 1, wc, kSitePEmpty)) {
-          tc_fence_after();
-          epilogue(m_fin, l_tot);
-        }
+        l_tot = l_other + (my_piece == epi_piece ? l_mine * exp2f(m_ref - m_fin) : 0.f);
+      }
+      if (go && wait_warp(bar(B_P_FREE + pp), ((t - 1) >> 1) & 1, wc, kSitePEmpty)) {
+        tc_fence_after();
+        epilogue(m_fin, l_tot, owner ? 1 : 0, 2);
       }
     }
   }
