@@ -307,18 +307,6 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
   const uint32_t half = cluster_ctarank(), peer = half ^ 1;
   const int unit = blockIdx.x >> 1;
 
-  // ---- unit record (uniform across the cluster); bail out early on bad metadata
-  const int32_t* sched = args.sched;
-  if (sched[0] != kSchedMagic || sched[1] != args.num_units || sched[2] != args.num_qb) {
-    if (tid == 0) atomicCAS(&g_mla_error, 0, 5);
-    return;
-  }
-  pdl_launch_dependents();  // the combine kernel may start launching; it waits for this grid to finish
-  const int32_t* rec = sched + kSchedHeader + kUnitInts * unit;
-  if (rec[0] < 0) return;  // no work for this unit (both CTAs take this path)
-  const int32_t* num_splits = sched + kSchedHeader + kUnitInts * args.num_units;
-  const int32_t* split_offset = num_splits + args.num_qb;
-
   auto bar = [&](uint32_t i) { return base + SM_BAR + 8 * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_BAR + OFF_ABORT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_BAR + OFF_TMEM_SLOT);
@@ -356,6 +344,23 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
   cluster_sync();  // peer barriers initialised before any remote arrive / st.async
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // Everything above touches no global memory: it runs while the kernel before this one in the
+  // stream is still finishing (programmatic dependent launch).  Its writes (the metadata, the
+  // inputs) are visible from here on.
+  pdl_wait_prerequisites();
+  // ---- unit record (uniform across the cluster); bail out early on bad metadata
+  const int32_t* sched = args.sched;
+  const bool bad_meta = sched[0] != kSchedMagic || sched[1] != args.num_units || sched[2] != args.num_qb;
+  const int32_t* rec = sched + kSchedHeader + kUnitInts * unit;
+  if (bad_meta || rec[0] < 0) {  // bad metadata, or no work for this unit (both CTAs take this path)
+    if (bad_meta && tid == 0) atomicCAS(&g_mla_error, 0, 5);
+    if (warp == 2) tmem_dealloc(tmem, 512);
+    return;
+  }
+  pdl_launch_dependents();  // the combine kernel may start launching; it waits for this grid to finish
+  const int32_t* num_splits = sched + kSchedHeader + kUnitInts * args.num_units;
+  const int32_t* split_offset = num_splits + args.num_qb;
 
   WaitCtx wc;
   wc.abort_local = abort_flag;

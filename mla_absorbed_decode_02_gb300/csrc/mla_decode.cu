@@ -400,7 +400,14 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cfg.numAttrs = 0;  // cluster shape comes from __cluster_dims__
+  // cluster shape from __cluster_dims__; programmatic dependent launch: the kernel's set-up
+  // (barriers, tensor memory) overlaps the end of the kernel before it in the stream, and it
+  // waits (griddepcontrol.wait) before reading any global memory
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   const cudaError_t e = a.kv_fp8 ? cudaLaunchKernelEx(&cfg, mla_decode_fp8_kernel, a)
                                  : cudaLaunchKernelEx(&cfg, mla_decode_bf16_kernel, a);
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
