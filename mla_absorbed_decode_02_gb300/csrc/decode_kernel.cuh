@@ -269,16 +269,26 @@ __device__ __forceinline__ void expand_fp8_stage(uint32_t sbase, int i, uint32_t
   float scale;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(scale) : "r"(sbase + kStageScales + row * 16 + (2 * half + part) * 4));
   asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+  // E4M3 -> bf16 without the conversion units: a code's 7 magnitude bits placed as a bf16's
+  // exponent and mantissa give the code's value times 2^-120 exactly (subnormal codes land on
+  // bf16 subnormals), the sign bit goes to bit 15; then x 2^120 (exact) and x scale (rounded
+  // to bf16) in two packed bf16 multiplies.
+  const uint32_t k120 = 0x7B807B80u;  // bf16x2 {2^120, 2^120}
+  uint32_t sc2;
+  {
+    const __nv_bfloat162 s2 = __floats2bfloat162_rn(scale, scale);
+    sc2 = *reinterpret_cast<const uint32_t*>(&s2);
+  }
 #pragma unroll
   for (int ch = 0; ch < 16; ++ch) {  // 8 codes -> 8 bf16 (16 bytes)
     uint32_t o[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint16_t two = (uint16_t)(c[2 * ch + (q >> 1)] >> (16 * (q & 1)));
-      uint32_t h2;
-      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-      o[q] = pack_bf16(f.x * scale, f.y * scale);
+      const uint32_t x = __byte_perm(c[2 * ch + (q >> 1)], 0u, (q & 1) ? 0x4342u : 0x4140u);  // codes in bytes 0, 2
+      const uint32_t y = ((x << 4) & 0x07F007F0u) | ((x << 8) & 0x80008000u);
+      uint32_t v;
+      asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(v) : "r"(y), "r"(k120));
+      asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[q]) : "r"(v), "r"(sc2));
     }
     const int blk = 2 * part + (ch >> 3), chunk = ch & 7;
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sbase + blk * kLatBlock + row * 128 +
