@@ -69,8 +69,9 @@ constexpr uint32_t kStageScales = 0;
 constexpr uint32_t kFp8StageTx = 64 * 256 + 4096 + 1024;  // codes + RoPE half + scales
 constexpr uint32_t kBf16StageTx = 4 * kLatBlock + 4096;   // latent half + RoPE half
 // P / exchange buffer of a tile parity: the peer's partial scores of tile t arrive here
-// ([8][128 rows][16 B]), are decoded, and P(t) ([128 rows x 128 B] bf16, 128-byte
-// swizzle) is written over them; the buffer is handed back to the peer once PV(t) is done.
+// ([8 column chunks][128 rows][16 B]), are decoded, and P(t) (bf16, same [8][128][16 B]
+// layout: K-major without swizzle for PV) is written over them, each thread on its own
+// row's chunks; the buffer is handed back to the peer once PV(t) is done.
 constexpr uint32_t kPBytes = kRows * 128;
 constexpr uint32_t SM_P = kStages * kStageBytes;      // P / exchange [tile parity]
 constexpr uint32_t SM_QR = SM_P + 2 * kPBytes;        // RoPE-query half [128 x 64 B], 64-byte swizzle
@@ -474,7 +475,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           const uint32_t sbase = base + st * kStageBytes;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint64_t a = smem_desc(base + SM_P + pb * kPBytes + k * 32, 16, 1024, kSwizzle128B);
+            const uint64_t a = smem_desc(base + SM_P + pb * kPBytes + k * 4096, 2048, 128, kSwizzleNone);
             const uint64_t bv = smem_desc(sbase + k * 2048, kLatBlock, 1024, kSwizzle128B);
             mma_bf16_ss(tmem + TM_O, a, bv, id_pv, (!ti.first || k > 0) ? 1u : 0u);
           }
@@ -695,7 +696,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
     if (kFp8 && w < n_tiles) ok = expand_tile(w);
     TileCursor cursor;
     cursor.init(walker0);
-    TileInfo x;
+    TileInfo x{};
     uint32_t t = 0;
     int piece = -1;
     // One tile of this warpgroup.  Two instances: the full one for the first and the last tile
@@ -825,18 +826,37 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           // the finished piece (last tile t-1) takes both warpgroups' row sums at its final max
           float epi_l = 0.f;
           if (kFull && epi_pending) epi_l = l_other + (my_piece == epi_piece ? l_mine * exp2f(m_ref - m_prev) : 0.f);
-          uint32_t pp[32];
+          // ---- the previous piece's epilogue (O after PV(t-1)), staged in this warpgroup's buffer
+          // once every thread has read its exchange data from it; P(t) goes there afterwards
+          if (kFull && epi_pending) {
+            asm volatile("bar.sync %0, 128;" ::"r"(1 + w) : "memory");
+            if (!(ok = wait_warp(bar(B_P_FREE + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSitePEmpty))) return false;
+            tc_fence_after();
+            epilogue(m_prev, epi_l, 0, 1);
+            epi_pending = false;
+            asm volatile("bar.sync %0, 128;" ::"r"(1 + w) : "memory");
+          }
+          // ---- exponentials; each thread stores its P row where it read its exchange data (16-byte
+          // chunk j of row r at (j * 128 + r) * 16: the K-major layout without swizzle that PV reads),
+          // so no thread writes where another still reads
           float rsum;
           {
             const uint64_t s2 = splat_f32x2(sl2), nm = splat_f32x2(-fmaf(beta, sl2, m));
             uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
   #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-              float x0, x1;
-              unpack_f32x2(ffma_f32x2(sc[u], s2, nm), x0, x1);
-              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-              pp[u] = pack_bf16(p0, p1);
-              acc[u & 3] = fadd_f32x2(acc[u & 3], pack_f32x2(p0, p1));
+            for (int j = 0; j < 8; ++j) {
+              uint32_t pp[4];
+  #pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int u = 4 * j + q;
+                float x0, x1;
+                unpack_f32x2(ffma_f32x2(sc[u], s2, nm), x0, x1);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                pp[q] = pack_bf16(p0, p1);
+                acc[q] = fadd_f32x2(acc[q], pack_f32x2(p0, p1));
+              }
+              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(my_x + (j * kRows + r) * 16), "r"(pp[0]),
+                           "r"(pp[1]), "r"(pp[2]), "r"(pp[3]));
             }
             float z[8];
             unpack_f32x2(fadd_f32x2(fadd_f32x2(acc[0], acc[1]), fadd_f32x2(acc[2], acc[3])), z[0], z[1]);
@@ -853,32 +873,22 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           ml[(sb * 2 + 1) * kRows + r] = l_mine;
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_ML + sb));
-          // ---- O is touched only after PV(t-1): the previous piece's epilogue, a rescale
-          const bool any_rescale = __any_sync(0xffffffffu, alpha != 1.f);
-          // every thread of the warpgroup has read its rows of the exchange data: from here the
-          // buffer takes the epilogue's staging and then P(t)
-          asm volatile("bar.sync %0, 128;" ::"r"(1 + w) : "memory");
-          if ((kFull && epi_pending) || any_rescale) {
+          // ---- a raised running max rescales O (after PV(t-1), before PV(t))
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
             if (!(ok = wait_warp(bar(B_P_FREE + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSitePEmpty))) return false;
             tc_fence_after();
-            if (kFull && epi_pending) {
-              epilogue(m_prev, epi_l, 0, 1);
-              epi_pending = false;
-            }
-            if (any_rescale) {
   #pragma unroll 1
-              for (int c = 0; c < 8; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_off + TM_O + 32 * c, v);
-                tmem_wait_ld();
+            for (int c = 0; c < 8; ++c) {
+              uint32_t v[32];
+              tmem_ld32(tmem + lane_off + TM_O + 32 * c, v);
+              tmem_wait_ld();
   #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-                tmem_st32(tmem + lane_off + TM_O + 32 * c, v);
-              }
-              tmem_wait_st();
+              for (int jj = 0; jj < 32; ++jj) v[jj] = __float_as_uint(__uint_as_float(v[jj]) * alpha);
+              tmem_st32(tmem + lane_off + TM_O + 32 * c, v);
             }
+            tmem_wait_st();
           }
-          // ---- publish P over the decoded exchange data (PV(t-2) was waited for above)
+          // ---- publish P
           if (kFull && valid < kTileTok) {
             // rows past the sequence end must not reach the PV product (0 * garbage): zero them
             const uint32_t sbase = base + (t % kStages) * kStageBytes;
@@ -889,11 +899,6 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
                            "r"(0u));
             }
           }
-          const uint32_t prow = base + SM_P + sb * kPBytes + r * 128;
-  #pragma unroll
-          for (int ch = 0; ch < 8; ++ch)  // P row: K-major, 128-byte swizzle
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((((uint32_t)ch) ^ (r & 7)) << 4)),
-                         "r"(pp[4 * ch]), "r"(pp[4 * ch + 1]), "r"(pp[4 * ch + 2]), "r"(pp[4 * ch + 3]));
           fence_proxy_async_smem();
           tc_fence_before();
           __syncwarp();

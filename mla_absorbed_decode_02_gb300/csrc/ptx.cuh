@@ -214,7 +214,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 // stride-dimension byte offsets (16-byte units), descriptor version 1,
 // base offset 0 (every swizzle atom we address is aligned to its own size),
 // swizzle mode in bits 61..63 (2 = 128-byte, 4 = 64-byte).
-enum : uint32_t { kSwizzle128B = 2, kSwizzle64B = 4 };
+enum : uint32_t { kSwizzleNone = 0, kSwizzle128B = 2, kSwizzle64B = 4 };
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
                                               uint32_t swizzle) {
   uint64_t d = 0;
