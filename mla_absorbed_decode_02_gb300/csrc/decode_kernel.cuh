@@ -78,7 +78,13 @@ constexpr uint32_t SM_QR = SM_P + 2 * kPBytes;        // RoPE-query half [128 x 
 constexpr uint32_t SM_XE = SM_QR + 8192;              // peer block-float exponents [tile parity][128 rows] u32
 constexpr uint32_t SM_ML = SM_XE + 2 * kRows * 4;     // published running max / row sum: [parity][2][128] f32
 constexpr uint32_t SM_BAR = SM_ML + 2 * 2 * kRows * 4;
-constexpr uint32_t kSmemBytes = SM_BAR + 512 + 1024;  // + alignment slack
+// Tile schedule the TMA producer publishes for the softmax warpgroups: one 32-byte entry per tile
+// in a ring of 8 ({qb, valid, split, flags (1 first, 2 last), piece, qb of the next piece or -1,
+// qb and split of the previous tile}); entry t is written after stage t-5 is free again, by
+// when the reader of entry t-8 has long read it.
+constexpr int kTiRing = 8;
+constexpr uint32_t SM_TI = SM_BAR + 512;
+constexpr uint32_t kSmemBytes = SM_TI + kTiRing * 32 + 1024;  // + alignment slack
 constexpr uint32_t kXBytes = kRows * (128 + 4);       // bytes one CTA sends the other per tile
 
 // tensor memory columns
@@ -101,7 +107,8 @@ enum : uint32_t {
   B_X_FULL = B_P_FREE + 2,          // [parity] the peer's partial scores of tile t arrived
   B_X_FREE = B_X_FULL + 2,          // [parity] the peer consumed what this CTA sent for tile t
   B_ML = B_X_FREE + 2,              // [parity] running max / row sum of tile t published
-  kNumBars = B_ML + 2
+  B_TI_FULL = B_ML + 2,             // [t mod 8] tile-schedule entry of tile t published
+  kNumBars = B_TI_FULL + kTiRing
 };
 constexpr uint32_t OFF_TMEM_SLOT = kNumBars * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
@@ -342,6 +349,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
       mbar_init(bar(B_X_FREE + p), 4);   // one remote arrival per warp of the peer's warpgroup p
       mbar_init(bar(B_ML + p), 4);
     }
+    for (int i = 0; i < kTiRing; ++i) mbar_init(bar(B_TI_FULL + i), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -401,6 +409,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
       TileCursor cur;
       cur.init(walker0);
       TileInfo ti;
+      PieceWalker ahead = walker0;  // one piece ahead of the tile walk
+      Piece np;
+      ahead.next(np);  // piece 0
+      int next_qb = -1, prev_qb = -1, prev_split = 0;
       uint32_t t = 0, piece_no = 0;
       while (cur.next(ti)) {
         if (ti.first) {
@@ -408,9 +420,22 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           mbar_arrive_expect_tx(bar(B_QR_FULL), 8192);
           tma_load_3d(base + SM_QR, &args.map_qr, bar(B_QR_FULL), 32 * half, 0, ti.qb, pol_q);
           ++piece_no;
+          next_qb = ahead.next(np) ? np.qb : -1;
         }
         const uint32_t st = t % kStages, ph = (t / kStages) & 1;
         if (!wait_one(bar(B_KV_EMPTY + st), ph ^ 1, wc, kSiteKvEmpty)) break;
+        {  // the tile's schedule entry for the softmax warpgroups
+          const uint32_t e = base + SM_TI + (t % kTiRing) * 32;
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(e), "r"(ti.qb), "r"(ti.valid), "r"(ti.split),
+                       "r"((ti.first ? 1 : 0) | (ti.last ? 2 : 0))
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(e + 16), "r"((int)piece_no - 1), "r"(next_qb),
+                       "r"(prev_qb), "r"(prev_split)
+                       : "memory");
+          mbar_arrive(bar(B_TI_FULL + (t % kTiRing)));
+          prev_qb = ti.qb;
+          prev_split = ti.split;
+        }
         const int b = ti.qb / args.s_q;
         const int page = args.block_table[(int64_t)b * args.max_pages + ti.tile];
         const uint32_t sbase = base + st * kStageBytes;
@@ -668,10 +693,12 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
       tc_fence_before();
     };
 
-    PieceWalker ahead = walker0;  // one piece ahead of the tile walk: feeds the query loads
-    Piece np;
-    bool has_np = ahead.next(np);  // piece 0
-    if (w == 0 && has_np) load_q_tmem(np.qb);
+    if (w == 0) {  // piece 0's query half
+      PieceWalker pw = walker0;
+      Piece p0;
+      if (pw.next(p0)) load_q_tmem(p0.qb);
+    }
+    int np_qb = -1;  // query block of the piece after the current tile's (from the schedule)
 
     float l_mine = 0.f, m_ref = 0.f;  // this warpgroup's part of the row sum, relative to m_ref
     uint32_t slot_dep = 0;            // computed from the last values read from the exchange slot
@@ -694,11 +721,30 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
       return true;
     };
     if (kFp8 && w < n_tiles) ok = expand_tile(w);
-    TileCursor cursor;
-    cursor.init(walker0);
     TileInfo x{};
     uint32_t t = 0;
     int piece = -1;
+    // the schedule entry of tile tt: x, piece, np_qb; and the epilogue the tile's warpgroup owes
+    // when tt opens a piece (the previous piece ended at tt-1)
+    auto read_entry = [&](uint32_t tt) {
+      const uint32_t e = base + SM_TI + (tt % kTiRing) * 32;
+      int v[8];
+      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(e) : "memory");
+      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]) : "r"(e + 16) : "memory");
+      x.qb = v[0];
+      x.valid = v[1];
+      x.split = v[2];
+      x.first = (v[3] & 1) != 0;
+      x.last = (v[3] & 2) != 0;
+      piece = v[4];
+      np_qb = v[5];
+      if (x.first && tt > 0) {
+        epi_pending = true;
+        epi_qb = v[6];
+        epi_split = v[7];
+        epi_piece = piece - 1;
+      }
+    };
     // One tile of this warpgroup.  Two instances: the full one for the first and the last tile
     // of a piece (query load for the next piece, the finished piece's epilogue, a partial last
     // page), and a lean one for the tiles in between, which carries none of that code -- the
@@ -714,12 +760,12 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           // tile 2 on, this warpgroup's buffer (P(t-2), read by PV(t-2)) is not handed back for X(t)
           // yet: the load is staged in it.  Before that the buffer may already be receiving.
           bool handed_back = false;
-          if (kFull && x.last && has_np) {
+          if (kFull && x.last && np_qb >= 0) {
             if (t < 2) {
-              load_q_tmem(np.qb);
+              load_q_tmem(np_qb);
             } else {
               if (!(ok = wait_warp(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) return false;
-              load_q_tmem_staged(np.qb);
+              load_q_tmem_staged(np_qb);
               if (lane == 0) mbar_arrive_remote(peer_bar0 + 8 * (B_X_FREE + sb));
               handed_back = true;
             }
@@ -906,31 +952,32 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           if (kFp8 && t + 2 < n_tiles && !(ok = expand_tile(t + 2))) return false;
       return true;
     };
-    while (ok && cursor.next(x)) {
-      if (x.first) {
-        ++piece;
-        has_np = ahead.next(np);  // the piece after this one
-        if (has_np && (t & 1) == w && r < H) {  // bring its query rows into L2 for the load at this piece's end
-          const char* qn = reinterpret_cast<const char*>(args.q_nope) + (((int64_t)np.qb * H + r) * 512 + 256 * half) * 2;
-          const char* qr = reinterpret_cast<const char*>(args.q_rope) + (((int64_t)np.qb * H + r) * 64 + 32 * half) * 2;
+    // this warpgroup's tiles: t = w, w + 2, ...
+    for (t = w; ok && t < n_tiles; t += 2) {
+      if (!(ok = wait_warp(bar(B_TI_FULL + (t % kTiRing)), (t / kTiRing) & 1, wc, kSiteSFull))) break;
+      read_entry(t);
+      if (x.first && np_qb >= 0 && r < H) {  // bring the next piece's query rows into L2 for its load
+        const char* qn = reinterpret_cast<const char*>(args.q_nope) + (((int64_t)np_qb * H + r) * 512 + 256 * half) * 2;
+        const char* qr = reinterpret_cast<const char*>(args.q_rope) + (((int64_t)np_qb * H + r) * 64 + 32 * half) * 2;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + 128 * k));
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(qr));
-        }
+        for (int k = 0; k < 4; ++k) asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + 128 * k));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qr));
       }
-      if ((t & 1) == w) {
-        if (!(x.first || x.last ? tile(std::true_type{}) : tile(std::false_type{}))) {
-          ok = false;
-          break;
-        }
+      if (!(x.first || x.last ? tile(std::true_type{}) : tile(std::false_type{}))) {
+        ok = false;
+        break;
       }
-      if (x.last) {  // the warpgroup of the next tile finishes this piece
-        epi_qb = x.qb;
-        epi_split = x.split;
-        epi_piece = piece;
-        epi_pending = ((t + 1) & 1) == w;
-      }
-      ++t;
+    }
+    // the unit's last tile n_tiles-1 (its entry is still in the ring): its piece ends the unit
+    t = n_tiles;
+    if (ok && t > 0) {
+      if (!(ok = wait_warp(bar(B_TI_FULL + ((t - 1) % kTiRing)), ((t - 1) / kTiRing) & 1, wc, kSiteSFull))) t = 0;
+      const bool pend = epi_pending;
+      read_entry(t - 1);
+      epi_pending = pend;
+      epi_qb = x.qb;
+      epi_split = x.split;
+      epi_piece = piece;
     }
     // The unit's last piece: both warpgroups write half of its columns each, from the same final
     // max and row sum (same operands, same operations).  The owner of the last tile t-1 takes the
