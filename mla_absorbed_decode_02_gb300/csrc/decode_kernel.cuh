@@ -963,7 +963,13 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
         for (int k = 0; k < 4; ++k) asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + 128 * k));
         asm volatile("prefetch.global.L2 [%0];" ::"l"(qr));
       }
-      if (!(x.first || x.last ? tile(std::true_type{}) : tile(std::false_type{}))) {
+      // (the lean instance first: it is the one the loop runs back to back)
+      if (__builtin_expect(!(x.first || x.last), 1)) {
+        if (!tile(std::false_type{})) {
+          ok = false;
+          break;
+        }
+      } else if (!tile(std::true_type{})) {
         ok = false;
         break;
       }
