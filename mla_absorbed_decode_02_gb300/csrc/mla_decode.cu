@@ -40,15 +40,16 @@ __global__ void __launch_bounds__(1024) mla_sched_kernel(const int32_t* seqlens,
 // out = sum_i exp(lse_i - lse) * out_i, lse = M + ln sum_i exp(lse_i - M), M = max_i lse_i
 // (the merge of split-KV partial results, "MLA inference: two computation paths and
 // FlashMLA", section "Decode attention becomes a compute problem").  Query blocks that see
-// no key get out = 0, lse = -inf.  One CTA of 256 threads per (query block, 16 heads): the
-// 16 combined LSEs first (two heads per warp, the splits spread over 16 lanes), then every
-// thread streams 8 float4 columns of one head per split, each split's 8 loads in flight together.
-constexpr int kCombineHeads = 16;
+// no key get out = 0, lse = -inf.  One CTA of 256 threads per (query block, 16 heads, 128
+// output columns): the 16 combined LSEs first (two heads per warp, the splits spread over
+// 16 lanes), then every thread streams 2 float4 columns of one head per split, four splits'
+// loads in flight together (a query block split across many units is merged by many CTAs).
+constexpr int kCombineHeads = 16, kCombineQuarters = 4;
 __global__ void __launch_bounds__(256) mla_combine_kernel(const int32_t* sched, int U, int NQB, int H,
                                                           const float* o_acc, const float* lse_acc, void* out,
                                                           float* lse, int out_f32) {
   pdl_wait_prerequisites();  // the decode kernel before it in the stream has finished
-  const int qb = blockIdx.x, h0 = blockIdx.y * kCombineHeads;
+  const int qb = blockIdx.x, h0 = blockIdx.y * kCombineHeads, quarter = blockIdx.z;
   const int32_t* num_splits = sched + kSchedHeader + kUnitInts * U;
   const int32_t* split_offset = num_splits + NQB;
   const int ns = num_splits[qb];
@@ -70,29 +71,44 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const int32_t* sched, 
     if (sub == 0) s_lse[hh] = M > -INFINITY ? M + logf(S) : -INFINITY;
   }
   __syncthreads();
-  const int hh = tid >> 4, h = h0 + hh, c = tid & 15;  // columns 4 (c + 16 k), k < 8
+  const int hh = tid >> 4, h = h0 + hh, c = 32 * quarter + (tid & 15);  // float4 columns c, c + 16
   if (h >= H) return;
   const float L = s_lse[hh];
-  float4 acc[8];
+  const int64_t split_stride = (int64_t)H * 128;  // float4 per split
+  const float4* src = reinterpret_cast<const float4*>(o_acc) + ((int64_t)off * H + h) * 128 + c;
+  const float* lsrc = lse_acc + (int64_t)off * H + h;
+  float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  auto add = [&](float wgt, const float4& v, float4& a) {
+    a.x += wgt * v.x;
+    a.y += wgt * v.y;
+    a.z += wgt * v.z;
+    a.w += wgt * v.w;
+  };
+  int i = 0;
+  for (; i + 4 <= ns; i += 4) {
+    float4 v[4][2];
+    float lw[4];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = 0; i < ns; ++i) {
-    const float wgt = expf(lse_acc[(int64_t)(off + i) * H + h] - L);
-    const float4* src = reinterpret_cast<const float4*>(o_acc + ((int64_t)(off + i) * H + h) * 512) + c;
-    float4 v[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) v[k] = __ldcs(src + 16 * k);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      acc[k].x += wgt * v[k].x;
-      acc[k].y += wgt * v[k].y;
-      acc[k].z += wgt * v[k].z;
-      acc[k].w += wgt * v[k].w;
+    for (int s = 0; s < 4; ++s) {
+      lw[s] = lsrc[(int64_t)(i + s) * H];
+      v[s][0] = __ldcs(src + (i + s) * split_stride);
+      v[s][1] = __ldcs(src + (i + s) * split_stride + 16);
     }
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const float wgt = expf(lw[s] - L);
+      add(wgt, v[s][0], acc[0]);
+      add(wgt, v[s][1], acc[1]);
+    }
+  }
+  for (; i < ns; ++i) {
+    const float wgt = expf(lsrc[(int64_t)i * H] - L);
+    add(wgt, __ldcs(src + i * split_stride), acc[0]);
+    add(wgt, __ldcs(src + i * split_stride + 16), acc[1]);
   }
   const int64_t row = (int64_t)qb * H + h;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < 2; ++k) {
     const int d = 4 * (c + 16 * k);
     if (out_f32) {
       *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + row * 512 + d) = acc[k];
@@ -103,7 +119,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const int32_t* sched, 
       *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + row * 512 + d) = o;
     }
   }
-  if (c == 0) lse[row] = L;
+  if ((tid & 15) == 0 && quarter == 0) lse[row] = L;
 }
 
 // ----------------------------------------------------------------- FP8 cache writer
@@ -430,7 +446,7 @@ int32_t mla_combine(const mla_decode_params* p, void* out, float* lse, const voi
   // programmatic dependent launch: this grid is set up while the decode kernel before it
   // drains, and waits (griddepcontrol.wait) for it before reading the partials
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(NQB, (H + kCombineHeads - 1) / kCombineHeads, 1);
+  cfg.gridDim = dim3(NQB, (H + kCombineHeads - 1) / kCombineHeads, kCombineQuarters);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = static_cast<cudaStream_t>(stream);
