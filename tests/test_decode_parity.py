@@ -154,6 +154,39 @@ def test_metadata_is_reusable_across_calls():
             BF16_TOL, "reused metadata", out_bf16=True)
 
 
+def test_decode_right_after_the_kernel_writing_its_queries():
+    """The decode kernel is launched as a programmatic dependent of the kernel before it on
+    the stream and starts its set-up early: it must still read the queries that kernel
+    writes.  A slow producer (a matmul) writes the queries immediately before the decode;
+    the result must be the oracle's for the new queries, not the old ones."""
+    import dataclasses
+    import torch
+    from mla_absorbed_decode_02_gb300 import Decoder, mla_device_error
+    w = mw.make_custom([2500, 900, 64, 4100], num_heads=128, seed=31)
+    w2 = mw.make_custom([2500, 900, 64, 4100], num_heads=128, seed=32)  # other queries (same shapes)
+    w2 = dataclasses.replace(w, q_nope=w2.q_nope, q_rope=w2.q_rope)      # same cache and pages as w
+    q_nope, q_rope, kv, bt, seq = to_device(w)
+    q2_nope, q2_rope, _, _, _ = to_device(w2)
+    dec = Decoder(params_for(w))
+    dec.plan(seq)
+    dec.decode(q_nope, q_rope, kv, bt, seq, w.scale)  # warm: the old queries' results
+    torch.cuda.synchronize()
+    # producer: q_nope <- q2_nope through a matmul that takes a while (x @ I, exact for bf16)
+    n = q2_nope.numel() // 512
+    eye = torch.eye(512, dtype=torch.bfloat16, device=q_nope.device)
+    big = torch.randn(8192, 8192, dtype=torch.bfloat16, device=q_nope.device)
+    for _ in range(3):
+        big = big @ big.T / 100.0  # keep the stream busy before the producer
+    q_rope.copy_(q2_rope)
+    torch.matmul(q2_nope.view(n, 512), eye, out=q_nope.view(n, 512))
+    out, lse = dec.decode(q_nope, q_rope, kv, bt, seq, w.scale)
+    torch.cuda.synchronize()
+    assert mla_device_error(clear=True) == 0
+    ref_out, ref_lse = oracle_full(w2, threads=THREADS)
+    compare(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ref_out, ref_lse,
+            BF16_TOL, "decode after its producer", out_bf16=True)
+
+
 # ------------------------------------------------------------------ FP8 E4M3 latent cache
 
 @pytest.mark.parametrize("num_units", [0, 3])
