@@ -262,18 +262,22 @@ __device__ __forceinline__ void st_async_b32(uint32_t cluster_dst, uint32_t v, u
                : "memory");
 }
 
-// FP8 cache: this warpgroup thread's share of a stage (i in [0, 128): row i/2, the 128 codes of tile
-// half i%2) -> bf16 x tile scale, written into the 128-byte-swizzled latent layout the MMAs read.
-// The codes sit in the upper half of the latent area, so every thread of the warpgroup reads its codes
-// before any thread writes (named barrier bar_id over the 128 threads).
+// FP8 cache: this warpgroup thread's share of a stage (i in [0, 128): row i % 64, the 128 codes of
+// tile half i / 64) -> bf16 x tile scale, written into the 128-byte-swizzled latent layout the MMAs
+// read.  A lane takes its eight 16-code chunks starting at chunk (lane mod 8): the eight lanes of a
+// quarter-warp then read eight different bank groups, and (rows consecutive across lanes, the
+// layout's row-XOR swizzle) write eight different ones -- no bank conflicts either way.  The codes
+// sit in the upper half of the latent area, so every thread of the warpgroup reads its codes before
+// any thread writes (named barrier bar_id over the 128 threads).
 __device__ __forceinline__ void expand_fp8_stage(uint32_t sbase, int i, uint32_t half, uint32_t bar_id) {
-  const int row = i >> 1, part = i & 1;
-  uint32_t c[32];
+  const int row = i & 63, part = i >> 6;
+  const uint32_t rot = (uint32_t)i & 7;
+  uint32_t c[32];  // c[4j .. 4j+3]: codes of chunk (j + rot) mod 8
 #pragma unroll
   for (int j = 0; j < 8; ++j)
     asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(c[4 * j]), "=r"(c[4 * j + 1]), "=r"(c[4 * j + 2]), "=r"(c[4 * j + 3])
-                 : "r"(sbase + kStageCodes + row * 256 + part * 128 + 16 * j));
+                 : "r"(sbase + kStageCodes + row * 256 + part * 128 + 16 * ((j + rot) & 7)));
   float scale;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(scale) : "r"(sbase + kStageScales + row * 16 + (2 * half + part) * 4));
   asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
@@ -288,7 +292,7 @@ __device__ __forceinline__ void expand_fp8_stage(uint32_t sbase, int i, uint32_t
     sc2 = *reinterpret_cast<const uint32_t*>(&s2);
   }
 #pragma unroll
-  for (int ch = 0; ch < 16; ++ch) {  // 8 codes -> 8 bf16 (16 bytes)
+  for (int ch = 0; ch < 16; ++ch) {  // 8 codes -> 8 bf16 (16 bytes): output chunk 2 ((j + rot) mod 8) + k
     uint32_t o[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -298,9 +302,10 @@ __device__ __forceinline__ void expand_fp8_stage(uint32_t sbase, int i, uint32_t
       asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(v) : "r"(y), "r"(k120));
       asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[q]) : "r"(v), "r"(sc2));
     }
-    const int blk = 2 * part + (ch >> 3), chunk = ch & 7;
+    const uint32_t out_ch = 2 * (((uint32_t)(ch >> 1) + rot) & 7) + (ch & 1);
+    const uint32_t blk = 2 * part + (out_ch >> 3), chunk = out_ch & 7;
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sbase + blk * kLatBlock + row * 128 +
-                                                              ((((uint32_t)chunk) ^ (row & 7)) << 4)),
+                                                              ((chunk ^ (uint32_t)(row & 7)) << 4)),
                  "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]));
   }
 }
