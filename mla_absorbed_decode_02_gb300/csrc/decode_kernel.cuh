@@ -708,8 +708,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
     float l_mine = 0.f, m_ref = 0.f;  // this warpgroup's part of the row sum, relative to m_ref
     uint32_t slot_dep = 0;            // computed from the last values read from the exchange slot
     int my_piece = -1;                // piece that l_mine belongs to
-    // FP8 cache: the warpgroup of tile t expands stage t to bf16 -- its first tile up front, tile
-    // t + 2 right after publishing P(t) -- so QK(t) finds a bf16 page.
+    // FP8 cache: stage t is expanded to bf16 before QK(t) -- tile 0 by warpgroup 0 and tiles 1 and 2
+    // by warpgroup 1 up front, tile t + 3 (the other warpgroup's next) by the warpgroup of tile t
+    // right after publishing P(t) -- so QK(t + 3) can run before that warpgroup is done with t + 1.
     uint32_t n_tiles = 0;  // tiles of this unit
     {
       PieceWalker pw = walker0;
@@ -725,7 +726,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
       if (lane == 0) mbar_arrive(bar(B_K_READY + st));
       return true;
     };
+    // (warpgroup 1 takes tile 2: warpgroup 0 must not wait for page 2 before tile 0, whose query
+    // load for the next piece the loading of page 2 may depend on)
     if (kFp8 && w < n_tiles) ok = expand_tile(w);
+    if (kFp8 && ok && w == 1 && 2 < n_tiles) ok = expand_tile(2);
     TileInfo x{};
     uint32_t t = 0;
     int piece = -1;
@@ -954,7 +958,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_P_FULL + sb));
-          if (kFp8 && t + 2 < n_tiles && !(ok = expand_tile(t + 2))) return false;
+          if (kFp8 && t + 3 < n_tiles && !(ok = expand_tile(t + 3))) return false;
       return true;
     };
     // this warpgroup's tiles: t = w, w + 2, ...
