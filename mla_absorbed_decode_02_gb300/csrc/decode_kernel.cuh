@@ -262,6 +262,14 @@ __device__ __forceinline__ void st_async_b32(uint32_t cluster_dst, uint32_t v, u
                : "memory");
 }
 
+// prmt with selector s on (x, 0): a selector nibble with bit 3 set replicates the sign bit of the
+// byte it selects (the PTX form; the __byte_perm intrinsic uses only the low 3 bits)
+__device__ __forceinline__ uint32_t prmt_sext(uint32_t x, uint32_t s) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(x), "r"(s));
+  return d;
+}
+
 // FP8 cache: this warpgroup thread's share of a stage (i in [0, 128): row i % 64, the 128 codes of
 // tile half i / 64) -> bf16 x tile scale, written into the 128-byte-swizzled latent layout the MMAs
 // read.  A lane takes its eight 16-code chunks starting at chunk (lane mod 8): the eight lanes of a
@@ -296,8 +304,10 @@ __device__ __forceinline__ void expand_fp8_stage(uint32_t sbase, int i, uint32_t
     uint32_t o[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint32_t x = __byte_perm(c[2 * ch + (q >> 1)], 0u, (q & 1) ? 0x4342u : 0x4140u);  // codes in bytes 0, 2
-      const uint32_t y = ((x << 4) & 0x07F007F0u) | ((x << 8) & 0x80008000u);
+      // two codes sign-extended to 16 bits (the byte permute's sign-replicate selectors), shifted so
+      // that the magnitude bits sit at bf16 bits 10..4, with the sign kept at bit 15
+      const uint32_t z = prmt_sext(c[2 * ch + (q >> 1)], (q & 1) ? 0xB3A2u : 0x9180u);
+      const uint32_t y = (z << 4) & 0x87F087F0u;
       uint32_t v;
       asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(v) : "r"(y), "r"(k120));
       asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[q]) : "r"(v), "r"(sc2));
