@@ -201,6 +201,50 @@ def test_fp8_two_new_tokens_causal():
     full_check(w, tol=FP8_TOL, num_units=4, what="fp8 s_q=2")
 
 
+def test_fp8_every_code_value_reaches_the_output_at_its_dimension():
+    """Each query selects one token of a shared page (orthogonal RoPE keys, no latent query; the
+    other tokens' scores are 115 nats lower, so their probabilities are exactly 0 in fp32) and
+    its output row is that token's dequantised latent row: e4m3(code) x tile scale. Rounding
+    allowed: the scale and the product to bf16, the output to bf16, and the selected token's
+    P = bf16(p) with p within a few 1e-3 of 1 (the 16-bit block floating point of the score
+    exchange is exact to ~2^-15 of the row's largest partial score, here 1600), so
+    |out - exact| <= 2^-6 |exact|; a misplaced code bit errs by 12% or more. Every non-NaN
+    code value sits at many dimensions of every row, under scales from 2^-120 (bf16
+    subnormal results) to 3e4."""
+    from oracle import e4m3_to_f64
+    T = 64
+    w = mw.make_custom([T] * T, num_heads=16, kv_dtype="fp8", seed=24)
+    w.block_table[:, 0] = w.block_table[0, 0]          # every sequence reads the same page
+    page = int(w.block_table[0, 0])
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)   # 254 values, no NaN
+    scales = np.array([1.0, 2.0 ** -120, 0.3716, 1234.5, 2.0 ** -118, 3.0e4, 7.0e-5, 0.1], np.float32)
+    sc_of = np.empty((T, 4), np.float32)
+    for j in range(T):
+        row = np.zeros(mw.FP8_ROW_BYTES, np.uint8)
+        row[:512] = codes[(np.arange(512) + 37 * j) % codes.size]
+        sc_of[j] = scales[(np.arange(4) + j) % scales.size]
+        row[512:528] = sc_of[j].view(np.uint8)
+        kr = np.zeros(mw.D_R, np.float32)
+        kr[j] = 40.0
+        row[528:656] = mw.to_bf16_bits(kr).view(np.uint8)
+        w.kv[page, j] = row
+    w.q_nope[:] = 0
+    qr = np.zeros((T, 1, 16, mw.D_R), np.float32)
+    qr[np.arange(T), 0, :, np.arange(T)] = 40.0        # sequence b selects token b
+    w.q_rope[:] = mw.to_bf16_bits(qr)
+    out, lse, _ = run_gpu(w, num_units=0)
+    value = np.array([e4m3_to_f64(c) for c in range(256)])
+    for b in range(T):
+        exact = value[w.kv[page, b, :512]] * np.repeat(sc_of[b].astype(np.float64), 128)
+        got = out[b, 0]                                  # [16 heads, 512]
+        err = np.abs(got - exact[None, :])
+        bound = np.abs(exact) * 2.0 ** -6 + 2.0 ** -133
+        bad = np.argwhere(err > bound[None, :])
+        assert bad.size == 0, (f"token {b}: dim {bad[0][1]} code {w.kv[page, b, bad[0][1]]:#04x} "
+                               f"got {got[tuple(bad[0])]!r} want {exact[bad[0][1]]!r}")
+    assert np.all(np.isfinite(lse))
+
+
 def test_fp8_row_garbage_past_the_end_is_ignored():
     """FP8 rows past the sequence end hold NaN codes, NaN scales and NaN RoPE: they must not leak."""
     w = mw.make_custom([65, 130, 1], num_heads=64, kv_dtype="fp8", seed=23)
