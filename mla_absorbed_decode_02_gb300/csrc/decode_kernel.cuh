@@ -738,8 +738,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
     };
     // (warpgroup 1 takes tile 2: warpgroup 0 must not wait for page 2 before tile 0, whose query
     // load for the next piece the loading of page 2 may depend on)
-    if (kFp8 && w < n_tiles) ok = expand_tile(w);
-    if (kFp8 && ok && w == 1 && 2 < n_tiles) ok = expand_tile(2);
+    if (kFp8) {
+#pragma unroll 1
+      for (uint32_t tt = w; ok && tt <= 2 * w && tt < n_tiles; ++tt) ok = expand_tile(tt);  // 0 | 1, 2
+    }
     TileInfo x{};
     uint32_t t = 0;
     int piece = -1;
