@@ -52,7 +52,7 @@ extern "C" {
 typedef enum {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned buffer */
-  MLA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (e.g. H > 128, s_q > 2) */
+  MLA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (e.g. H > 128, s_q > 8) */
   MLA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed (no device, launch failure, ...) */
   MLA_ERR_TIMEOUT = 4,      /* device error word: a bounded wait inside a kernel ran out */
   MLA_ERR_WORKSPACE = 5,    /* scheduler metadata does not match the params (wrong unit count or batch) */
@@ -73,7 +73,8 @@ typedef enum {
 /* Problem description shared by all calls of one decode step. */
 typedef struct mla_decode_params {
   int32_t batch;             /* B >= 1 sequences */
-  int32_t s_q;               /* new tokens per sequence: 1 or 2 */
+  int32_t s_q;               /* new tokens per sequence, 1..8 (MTP / speculative decoding); each
+                                new token is its own query block of H rows */
   int32_t num_heads;         /* H, 1..128 query heads */
   int32_t num_pages;         /* physical pages in the pool (>= 1) */
   int32_t page_size;         /* tokens per page; must be 64 */

@@ -251,7 +251,7 @@ int32_t check_params(const mla_decode_params* p) {
     if (p->reserved[i] != 0) return MLA_ERR_INVALID_ARG;
   if (p->kv_dtype != MLA_KV_BF16 && p->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
   if (p->out_dtype != MLA_OUT_BF16 && p->out_dtype != MLA_OUT_F32) return MLA_ERR_INVALID_ARG;
-  if (p->page_size != 64 || p->s_q > 2 || p->num_heads > 128) return MLA_ERR_UNSUPPORTED;
+  if (p->page_size != 64 || p->s_q > 8 || p->num_heads > 128) return MLA_ERR_UNSUPPORTED;
   if ((int64_t)p->batch * p->s_q > (1 << 24) || (int64_t)p->num_pages * 64 > INT32_MAX) return MLA_ERR_UNSUPPORTED;
   return MLA_OK;
 }

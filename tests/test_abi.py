@@ -57,7 +57,7 @@ def test_workspace_size_without_gpu(lib):
 @pytest.mark.parametrize("kw,status", [
     (dict(batch=0), _lib.MLA_ERR_INVALID_ARG),
     (dict(num_heads=129), _lib.MLA_ERR_UNSUPPORTED),
-    (dict(s_q=3), _lib.MLA_ERR_UNSUPPORTED),
+    (dict(s_q=9), _lib.MLA_ERR_UNSUPPORTED),
     (dict(page_size=32), _lib.MLA_ERR_UNSUPPORTED),
     (dict(kv_dtype=7), _lib.MLA_ERR_INVALID_ARG),
     (dict(out_dtype=5), _lib.MLA_ERR_INVALID_ARG),
@@ -119,7 +119,7 @@ def decode_plan(sched, B, s_q, causal, seqlens):
 def test_plan_covers_every_tile_once(lib, seed):
     rng = np.random.default_rng(seed)
     B = int(rng.integers(1, 80))
-    s_q = int(rng.integers(1, 3))
+    s_q = int(rng.integers(1, 9))
     causal = bool(rng.integers(0, 2))
     kind = seed % 4
     if kind == 0:

@@ -88,6 +88,19 @@ def test_two_new_tokens(causal):
     full_check(w, num_units=4, what=f"s_q=2 causal={causal}")
 
 
+@pytest.mark.parametrize("s_q,causal", [(4, True), (8, True), (8, False)])
+def test_up_to_eight_new_tokens(s_q, causal):
+    """MTP / speculative decoding: s_q new tokens per sequence, each its own query block.
+    Sequences shorter than s_q leave the first causal tokens with no visible key."""
+    w = mw.make_custom([1, 3, 8, 9, 65, 300, 1000], num_heads=128, s_q=s_q, causal=causal, seed=40 + s_q)
+    full_check(w, num_units=5, what=f"s_q={s_q} causal={causal}")
+
+
+def test_fp8_cache_four_new_tokens():
+    w = mw.make_custom([4, 70, 640], num_heads=64, s_q=4, causal=True, kv_dtype="fp8", seed=49)
+    full_check(w, tol=FP8_TOL, num_units=3, what="fp8 s_q=4")
+
+
 def test_empty_sequences():
     w = mw.make_custom([0, 100, 0, 1], num_heads=32, seed=15)
     out, lse, _ = run_gpu(w, num_units=2)

@@ -125,7 +125,7 @@ def test_brute_force_tiny(seed):
     rng = np.random.default_rng(seed)
     B = int(rng.integers(1, 4))
     H = int(rng.integers(1, 5))
-    s_q = int(rng.integers(1, 3))
+    s_q = int(rng.integers(1, 9))
     causal = bool(rng.integers(0, 2))
     d_c, d_r, page = 32, 8, 16
     Ls = rng.integers(s_q, 131, size=B)
