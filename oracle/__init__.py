@@ -51,23 +51,29 @@ _lib = None
 _lock = threading.Lock()
 
 
+def bind(path: str):
+    """Load an oracle library build (the normal one, or a test's variant of the same source)
+    and declare its entry points."""
+    lib = ctypes.CDLL(path)
+    lib.orc_decode_rows.argtypes = [ctypes.POINTER(_Problem), ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                    ctypes.c_void_p]
+    lib.orc_decode_rows.restype = ctypes.c_int
+    lib.orc_merge.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                              ctypes.c_void_p, ctypes.c_void_p]
+    lib.orc_merge.restype = None
+    lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    lib.orc_e4m3_to_f64.restype = ctypes.c_double
+    lib.orc_visible_keys.argtypes = [ctypes.POINTER(_Problem), ctypes.c_int, ctypes.c_int]
+    lib.orc_visible_keys.restype = ctypes.c_int
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            lib.orc_decode_rows.argtypes = [ctypes.POINTER(_Problem), ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
-                                            ctypes.c_void_p]
-            lib.orc_decode_rows.restype = ctypes.c_int
-            lib.orc_merge.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
-                                      ctypes.c_void_p, ctypes.c_void_p]
-            lib.orc_merge.restype = None
-            lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
-            lib.orc_e4m3_to_f64.restype = ctypes.c_double
-            lib.orc_visible_keys.argtypes = [ctypes.POINTER(_Problem), ctypes.c_int, ctypes.c_int]
-            lib.orc_visible_keys.restype = ctypes.c_int
-            _lib = lib
+            _lib = bind(build())
     return _lib
 
 
