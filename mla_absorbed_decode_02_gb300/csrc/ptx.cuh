@@ -100,17 +100,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
       : "memory");
 }
-// Bring a tensor-map box into L2 (no shared memory, no completion signal).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y, uint64_t policy) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;" ::"l"(map), "r"(x),
-               "r"(y), "l"(policy)
-               : "memory");
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
 // 16-byte global store with an L2 eviction-priority hint.
 __device__ __forceinline__ void st_global_v4_hint(void* ptr, float4 v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "f"(v.x), "f"(v.y), "f"(v.z),
