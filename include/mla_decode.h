@@ -117,6 +117,9 @@ int32_t mla_get_scheduler_metadata(const mla_decode_params* p, const int32_t* ca
  *                    sequence b; entries past ceil(L_b/64) are never read.  Every entry read
  *                    must be in [0, num_pages).
  *   cache_seqlens    device int32 [B]; L_b includes the s_q new tokens; 0 <= L_b <= 64*max_pages
+ *                    (a longer length sets MLA_ERR_INVALID_ARG in the device error word; the
+ *                    kernel then reads no block-table entry past the row, and that sequence's
+ *                    result is undefined)
  *   scale            softmax scale, finite and > 0 (1/sqrt(192) for DeepSeek-V3 shapes)
  *   out              device [B][s_q][H][512], bf16 or float32 (out_dtype)
  *   lse              device float32 [B][s_q][H]; a token that sees no key gets out = 0, lse = -inf
@@ -176,7 +179,9 @@ int32_t mla_quantize_kv_fp8(const void* kv_bf16, void* kv_fp8, int64_t num_token
 
 /*
  * Device error word of the current device: synchronises the device, writes the
- * word to *word (MLA_OK if none; MLA_ERR_TIMEOUT + 16 * site otherwise) and,
+ * word to *word (MLA_OK if none; MLA_ERR_TIMEOUT + 16 * site for a bounded wait that ran
+ * out; MLA_ERR_INVALID_ARG for a length beyond the block table; MLA_ERR_WORKSPACE for
+ * scheduler metadata that does not match the params) and,
  * if clear != 0, resets it.  Host pointer.
  */
 int32_t mla_device_error(int32_t* word, int32_t clear);

@@ -452,7 +452,12 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           prev_split = ti.split;
         }
         const int b = ti.qb / args.s_q;
-        const int page = args.block_table[(int64_t)b * args.max_pages + ti.tile];
+        int lp = ti.tile;  // logical page
+        if (lp >= args.max_pages) {  // a length beyond the block table: reported; no read past the row
+          atomicCAS(&g_mla_error, 0, 1);
+          lp = args.max_pages - 1;
+        }
+        const int page = args.block_table[(int64_t)b * args.max_pages + lp];
         const uint32_t sbase = base + st * kStageBytes;
         if (kFp8) {  // 656-byte rows: codes of this half, its RoPE half, the 4 tile scales
           mbar_arrive_expect_tx(bar(B_KV_FULL + st), kFp8StageTx);

@@ -109,6 +109,25 @@ def test_empty_sequences():
     assert np.all(lse[0] == -np.inf) and np.all(out[0] == 0) and np.all(lse[2] == -np.inf)
 
 
+def test_length_beyond_the_block_table_is_reported():
+    """A length past 64 x max_pages_per_seq breaks the call's contract: the decode reports
+    MLA_ERR_INVALID_ARG in the device error word, reads nothing past the block-table row, and
+    the other sequences' results are still right."""
+    import torch
+    from mla_absorbed_decode_02_gb300 import Decoder, MLA_ERR_INVALID_ARG, mla_device_error
+    w = mw.make_custom([100, 128], num_heads=128, seed=25)       # block table rows of 2 pages
+    ref_out, ref_lse = oracle_full(w)
+    q_nope, q_rope, kv, bt, seq = to_device(w)
+    seq[1] = 300                                                  # 5 pages, 3 past the row
+    dec = Decoder(params_for(w, num_units=3))
+    dec.plan(seq)
+    out, lse = dec.decode(q_nope, q_rope, kv, bt, seq, w.scale)
+    torch.cuda.synchronize()
+    assert mla_device_error(clear=True) == MLA_ERR_INVALID_ARG
+    compare(out[:1].float().cpu().numpy().astype(np.float64), lse[:1].cpu().numpy().astype(np.float64),
+            ref_out[:1], ref_lse[:1], BF16_TOL, "valid sequence next to an overlong one", out_bf16=True)
+
+
 def test_all_pages_alias_one_physical_page():
     w = mw.make_custom([300, 64, 129], num_heads=128, seed=16)
     w.block_table[w.block_table >= 0] = 0
