@@ -52,7 +52,7 @@ extern "C" {
 typedef enum {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned buffer */
-  MLA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (e.g. H > 128, s_q > 8) */
+  MLA_ERR_UNSUPPORTED = 2,  /* valid request the library does not implement (e.g. H > 128, s_q > 8) */
   MLA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed (no device, launch failure, ...) */
   MLA_ERR_TIMEOUT = 4,      /* device error word: a bounded wait inside a kernel ran out */
   MLA_ERR_WORKSPACE = 5,    /* scheduler metadata does not match the params (wrong unit count or batch) */
