@@ -254,12 +254,117 @@ def cpu_baseline(w, peaks, budget_s: float, threads: int):
 
 
 # ------------------------------------------------------------------ our arm
+def _device_inputs(w, dev):
+    import torch
+    host = {
+        "q_nope": torch.from_numpy(w.q_nope.view(np.int16)).view(torch.bfloat16),
+        "q_rope": torch.from_numpy(w.q_rope.view(np.int16)).view(torch.bfloat16),
+        "kv": (torch.from_numpy(w.kv.view(np.int16)).view(torch.bfloat16) if w.kv_dtype == "bf16"
+               else torch.from_numpy(w.kv)),
+        "bt": torch.from_numpy(w.block_table),
+        "seq": torch.from_numpy(w.seqlens),
+    }
+    return host, {k: v.to(dev) for k, v in host.items()}
+
+
+def _params(w):
+    from mla_absorbed_decode_02_gb300 import (MlaDecodeParams, MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_OUT_BF16,
+                                              MLA_OUT_F32)
+    return MlaDecodeParams.make(w.batch, w.s_q, w.num_heads, w.num_pages, w.block_table.shape[1], causal=w.causal,
+                                kv_dtype=MLA_KV_FP8_E4M3 if w.kv_dtype == "fp8" else MLA_KV_BF16,
+                                out_dtype=MLA_OUT_F32 if w.out_dtype == "f32" else MLA_OUT_BF16)
+
+
+def _accounting(w, peaks):
+    flops = algorithmic_flops(w.seqlens, w.s_q, w.num_heads, w.causal)
+    row_bytes = 656 if w.kv_dtype == "fp8" else 1152
+    nbytes = algorithmic_bytes(w.seqlens, w.s_q, w.num_heads, row_bytes, 4 if w.out_dtype == "f32" else 2)
+    t_roof, bound = roofline_time_s(flops, nbytes, peaks)
+    return flops, nbytes, row_bytes, t_roof, bound
+
+
+def _roofline(w, name, peaks, t_dec):
+    """Roofline object of the decode kernel: algorithmic bytes (or FLOPs) per launch over its event time."""
+    flops, nbytes, _, _, bound = _accounting(w, peaks)
+    if bound == "hbm":
+        achieved = nbytes / t_dec / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} (copy, burst)"}
+    else:
+        achieved = flops / t_dec / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "peak_source": f"{peaks['source']} (cuBLAS bf16, burst)"}
+    roof["traffic"] = committed_traffic(name)
+    roof["kernel"] = "mla_decode_fp8_kernel" if w.kv_dtype == "fp8" else "mla_decode_bf16_kernel"
+    roof["kernel_ms"] = t_dec * 1e3
+    return roof
+
+
+def time_workload(w, name, peaks, steps, warmup, dev, flush, dist=None):
+    """Device timing of one workload, inputs resident in HBM, L2 flushed before every step.
+
+    Pass 1 times whole steps (decode kernel + LSE combine, nothing between the two launches, so
+    the combine starts as a programmatic dependent of the decode kernel); pass 2 times the decode
+    kernel alone (an event right after it).  Both report the median over `steps` steps after
+    `warmup` untimed ones."""
+    import torch
+    from mla_absorbed_decode_02_gb300 import (Decoder, mla_combine, mla_decode_splitkv, mla_device_error,
+                                              mla_get_scheduler_metadata)
+    host, d = _device_inputs(w, dev)
+    p = _params(w)
+    dec = Decoder(p, dev)
+    out, lse = dec.new_outputs()
+    stream = torch.cuda.current_stream(dev)
+    mla_get_scheduler_metadata(p, d["seq"], dec.sched, stream)
+
+    def decode():
+        mla_decode_splitkv(p, d["q_nope"], d["q_rope"], d["kv"], d["bt"], d["seq"], w.scale, out, lse, dec.sched,
+                           dec.workspace, stream)
+
+    def combine():
+        mla_combine(p, out, lse, dec.sched, dec.workspace, stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        decode()
+        combine()
+    torch.cuda.synchronize(dev)
+    assert mla_device_error(clear=True) == 0, "device error during warm-up"
+
+    def timed(kernel_only):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        for k in range(steps):
+            flush.zero_()
+            evs[k][0].record(stream)
+            decode()
+            if kernel_only:
+                evs[k][1].record(stream)
+                combine()
+            else:
+                combine()
+                evs[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        return [a.elapsed_time(b) / 1e3 for a, b in evs]
+
+    step_s = timed(False)
+    dec_s = timed(True)
+    err = mla_device_error(clear=True)
+    assert err == 0, f"device error word {err}"
+    res = {"t_step": statistics.median(step_s), "t_step_mean": sum(step_s) / len(step_s),
+           "t_dec": statistics.median(dec_s), "host": host, "dev": d, "p": p, "dec": dec, "out": out, "lse": lse}
+    return res
+
+
 def run_ours(args, w, peaks, world, rank, local):
     import torch
+    import mla_workloads as mw
     from mla_absorbed_decode_02_gb300.build import build
-    from mla_absorbed_decode_02_gb300 import (Decoder, MlaDecodeParams, MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_OUT_BF16,
-                                              MLA_OUT_F32, mla_combine, mla_decode, mla_decode_splitkv,
-                                              mla_device_error, mla_get_scheduler_metadata)
+    from mla_absorbed_decode_02_gb300 import mla_decode, mla_device_error, mla_get_scheduler_metadata
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if rank == 0 or world == 1:
@@ -268,78 +373,34 @@ def run_ours(args, w, peaks, world, rank, local):
     if dist is not None:
         dist.barrier()
         build()
-
-    q_nope_h = torch.from_numpy(w.q_nope.view(np.int16)).view(torch.bfloat16)
-    q_rope_h = torch.from_numpy(w.q_rope.view(np.int16)).view(torch.bfloat16)
-    kv_h = torch.from_numpy(w.kv.view(np.int16)).view(torch.bfloat16) if w.kv_dtype == "bf16" else torch.from_numpy(w.kv)
-    bt_h = torch.from_numpy(w.block_table)
-    seq_h = torch.from_numpy(w.seqlens)
-    q_nope, q_rope, kv = q_nope_h.to(dev), q_rope_h.to(dev), kv_h.to(dev)
-    bt, seq = bt_h.to(dev), seq_h.to(dev)
-    p = MlaDecodeParams.make(w.batch, w.s_q, w.num_heads, w.num_pages, w.block_table.shape[1], causal=w.causal,
-                             kv_dtype=MLA_KV_FP8_E4M3 if w.kv_dtype == "fp8" else MLA_KV_BF16,
-                             out_dtype=MLA_OUT_F32 if w.out_dtype == "f32" else MLA_OUT_BF16)
-    dec = Decoder(p, dev)
-    out, lse = dec.new_outputs()
-    stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # > L2 (129 MB)
+    stream = torch.cuda.current_stream(dev)
 
-    mla_get_scheduler_metadata(p, seq, dec.sched, stream)
-
-    def step(ev=None):
-        if ev is None:
-            mla_decode_splitkv(p, q_nope, q_rope, kv, bt, seq, w.scale, out, lse, dec.sched, dec.workspace, stream)
-            mla_combine(p, out, lse, dec.sched, dec.workspace, stream)
-            return
-        ev[0].record(stream)
-        mla_decode_splitkv(p, q_nope, q_rope, kv, bt, seq, w.scale, out, lse, dec.sched, dec.workspace, stream)
-        ev[1].record(stream)
-        mla_combine(p, out, lse, dec.sched, dec.workspace, stream)
-        ev[2].record(stream)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize(dev)
-    assert mla_device_error(clear=True) == 0, "device error during warm-up"
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.3)
-    for k in range(args.steps):
-        flush.zero_()
-        step(evs[k])
-    torch.cuda.synchronize(dev)
-    if dist is not None:
-        dist.barrier()
+    r = time_workload(w, args.workload, peaks, args.steps, args.warmup, dev, flush, dist)
     clk = clocks.stop()
-    err = mla_device_error(clear=True)
-    assert err == 0, f"device error word {err}"
-    step_ms = [evs[k][0].elapsed_time(evs[k][2]) for k in range(args.steps)]
-    dec_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(args.steps)]
-    t_step = sum(step_ms) / len(step_ms) / 1e3
-    t_dec = sum(dec_ms) / len(dec_ms) / 1e3
+    t_step, t_dec = r["t_step"], r["t_dec"]
     t_max = reduce_max(t_step, dist, dev)
 
     # ---- end to end through the public API: pinned host inputs -> device, plan, decode, results -> host
-    pin = lambda t: t.pin_memory()
-    hq, hr, hbt, hseq = pin(q_nope_h), pin(q_rope_h), pin(bt_h), pin(seq_h)
+    host, d, p, dec, out, lse = r["host"], r["dev"], r["p"], r["dec"], r["out"], r["lse"]
+    units = dec.num_units
+    hq, hr, hbt, hseq = (host[k].pin_memory() for k in ("q_nope", "q_rope", "bt", "seq"))
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hq, hr, hbt, hseq))
     d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
 
     def e2e_step():
-        q_nope.copy_(hq, non_blocking=True)
-        q_rope.copy_(hr, non_blocking=True)
-        bt.copy_(hbt, non_blocking=True)
-        seq.copy_(hseq, non_blocking=True)
-        mla_get_scheduler_metadata(p, seq, dec.sched, stream)
-        mla_decode(p, q_nope, q_rope, kv, bt, seq, w.scale, out, lse, dec.sched, dec.workspace, stream)
+        d["q_nope"].copy_(hq, non_blocking=True)
+        d["q_rope"].copy_(hr, non_blocking=True)
+        d["bt"].copy_(hbt, non_blocking=True)
+        d["seq"].copy_(hseq, non_blocking=True)
+        mla_get_scheduler_metadata(p, d["seq"], dec.sched, stream)
+        mla_decode(p, d["q_nope"], d["q_rope"], d["kv"], d["bt"], d["seq"], w.scale, out, lse, dec.sched,
+                   dec.workspace, stream)
         hout.copy_(out, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
 
@@ -356,26 +417,13 @@ def run_ours(args, w, peaks, world, rank, local):
         b.record(stream)
         b.synchronize()
         e_ms.append(a.elapsed_time(b))
-    t_e2e = reduce_max(sum(e_ms) / len(e_ms) / 1e3, dist, dev)
+    t_e2e = reduce_max(statistics.median(e_ms) / 1e3, dist, dev)
     assert mla_device_error(clear=True) == 0
+    del r, host, d, dec, out, lse
 
-    flops = algorithmic_flops(w.seqlens, w.s_q, w.num_heads, w.causal)
-    row_bytes = 656 if w.kv_dtype == "fp8" else 1152
-    nbytes = algorithmic_bytes(w.seqlens, w.s_q, w.num_heads, row_bytes, 4 if w.out_dtype == "f32" else 2)
-    t_roof, bound = roofline_time_s(flops, nbytes, peaks)
+    flops, nbytes, row_bytes, t_roof, bound = _accounting(w, peaks)
     n = world
     value = 100.0 * n * t_roof / t_max
-    if bound == "hbm":
-        achieved = nbytes / t_dec / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} (copy, burst)"}
-    else:
-        achieved = flops / t_dec / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "peak_source": f"{peaks['source']} (cuBLAS bf16, burst)"}
-    roof["traffic"] = committed_traffic(args.workload)
-    roof["kernel"] = "mla_decode_fp8_kernel" if w.kv_dtype == "fp8" else "mla_decode_bf16_kernel"
-    roof["kernel_ms"] = t_dec * 1e3
     res = {
         "metric": METRIC, "value": value, "unit": "% of GB300 roofline (summed over GPUs)", "n_gpus": n,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max * 1e3, "higher_is_better": True,
@@ -383,10 +431,11 @@ def run_ours(args, w, peaks, world, rank, local):
         "data": "synthetic (seeded N(0,1) bf16 queries and cache, random page permutation)",
         "config": {"workload": args.workload, "batch": w.batch, "heads": w.num_heads, "s_q": w.s_q,
                    "seqlens": f"{int(w.seqlens.min())}..{int(w.seqlens.max())} (sum {int(w.seqlens.sum())})",
-                   "kv_dtype": w.kv_dtype, "pages": w.num_pages, "units": dec.num_units,
-                   "l2": "flushed before every step (256 MiB write)", "parallelism": f"replicas x{n}"},
+                   "kv_dtype": w.kv_dtype, "pages": w.num_pages, "units": units,
+                   "l2": "flushed before every step (256 MiB write)", "parallelism": f"replicas x{n}",
+                   "timing": f"median of {args.steps} steps after {args.warmup} warm-up steps, CUDA events"},
         "tflops": n * flops / t_max / 1e12, "kv_gbs": n * kv_bytes(w.seqlens, row_bytes) / t_max / 1e9,
-        "roofline": roof,
+        "roofline": _roofline(w, args.workload, peaks, t_dec),
         "e2e": {"value": 100.0 * n * t_roof / t_e2e, "unit": "% of GB300 roofline (summed over GPUs)",
                 "ms_per_step": t_e2e * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "includes": "H2D q/q_rope/block_table/seqlens, scheduler metadata, decode, D2H out/lse"},
@@ -394,18 +443,42 @@ def run_ours(args, w, peaks, world, rank, local):
         "clocks": clk,
         "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops", "source")},
     }
+
+    # ---- the other benchmark workloads (one GPU: the driver's multi-GPU runs time the headline only)
+    if world == 1 and not args.no_per_config:
+        per = {}
+        clocks = ClockSampler(local)
+        clocks.start()
+        time.sleep(0.3)
+        for name in ("uniform4k", "long", "fp8_mtp2"):
+            if name == args.workload:
+                continue
+            wk = mw.make_workload(WORKLOAD_INDEX[name])
+            rk = time_workload(wk, name, peaks, args.steps, args.warmup, dev, flush)
+            _, _, _, tr, _ = _accounting(wk, peaks)
+            per[name] = {"value": 100.0 * tr / rk["t_step"], "ms_per_step": rk["t_step"] * 1e3,
+                         "kernel_ms": rk["t_dec"] * 1e3, "roofline": _roofline(wk, name, peaks, rk["t_dec"]),
+                         "config": {"batch": wk.batch, "s_q": wk.s_q, "kv_dtype": wk.kv_dtype,
+                                    "seqlens": f"{int(wk.seqlens.min())}..{int(wk.seqlens.max())} "
+                                               f"(sum {int(wk.seqlens.sum())})"}}
+            del rk, wk
+            torch.cuda.empty_cache()
+        per_clk = clocks.stop()
+        res["per_config"] = per
+        res["per_config_clocks"] = per_clk
     return res, dist
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="ragged", choices=sorted(WORKLOAD_INDEX))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="time the chosen workload only")
     args = ap.parse_args()
     import mla_workloads as mw
 

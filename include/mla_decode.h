@@ -119,7 +119,8 @@ int32_t mla_get_scheduler_metadata(const mla_decode_params* p, const int32_t* ca
  *   cache_seqlens    device int32 [B]; L_b includes the s_q new tokens; 0 <= L_b <= 64*max_pages
  *                    (a longer length sets MLA_ERR_INVALID_ARG in the device error word; the
  *                    kernel then reads no block-table entry past the row, and that sequence's
- *                    result is undefined)
+ *                    result is undefined; a negative length sets the same error and is decoded
+ *                    as an empty sequence)
  *   scale            softmax scale, finite and > 0 (1/sqrt(192) for DeepSeek-V3 shapes)
  *   out              device [B][s_q][H][512], bf16 or float32 (out_dtype)
  *   lse              device float32 [B][s_q][H]; a token that sees no key gets out = 0, lse = -inf
@@ -154,9 +155,16 @@ int32_t mla_combine(const mla_decode_params* p, void* out, float* lse, const voi
  * for tests and capacity planning.  cache_seqlens and sched are HOST pointers;
  * num_units must be >= 1; sched must hold sched_bytes for that unit count.
  * Layout of sched (int32): [0] = 0x4D4C4131, [1] = units, [2] = B*s_q query blocks,
- * [3] = partial slots used, [4..7] = 0; then per unit 8 ints {qb_begin, tile_begin,
- * qb_end, tile_end (exclusive), first_split, 0, 0, 0} (qb_begin = -1: no work); then
- * num_splits[B*s_q]; then split_offset[B*s_q].  A query block qb = b*s_q + t.
+ * [3] = partial slots used, [4] = per-unit budget of work positions (one per 64-key
+ * tile plus a fixed cost per query block; diagnostic), [5..7] = 0; then per unit 8
+ * ints {qb_begin, tile_begin, qb_end, tile_end (exclusive), first_split, 0, 0, 0}
+ * (qb_begin = -1: no work); then num_splits[B*s_q]; then split_offset[B*s_q].  A query
+ * block qb = b*s_q + t.
+ * Returns MLA_ERR_INVALID_ARG for a negative length, or for lengths whose work
+ * positions exceed 2^31 - 1 in total (sched then holds a header without the magic
+ * word).  The scheduler kernel (mla_get_scheduler_metadata) reports the same two
+ * cases in the device error word: it plans a negative length as an empty sequence,
+ * and for the oversized case writes that invalid header, so the decode writes nothing.
  */
 int32_t mla_plan_host(const mla_decode_params* p, int32_t num_units, const int32_t* cache_seqlens, void* sched);
 

@@ -26,9 +26,19 @@ __global__ void __launch_bounds__(1024) mla_sched_kernel(const int32_t* seqlens,
   int32_t* num_splits = units + kUnitInts * U;
   int32_t* pos = num_splits + NQB;  // scratch until the last phase
   plan_phase_cost(seqlens, s_q, causal, NQB, pos, tid, nt);
+  // a negative length is outside the contract: reported, and planned as an empty sequence
+  for (int b = tid; b < B; b += nt)
+    if (seqlens[b] < 0) atomicCAS(&g_mla_error, 0, MLA_ERR_INVALID_ARG);
   __syncthreads();
   if (tid == 0) sh_total = plan_phase_scan(pos, NQB);
   __syncthreads();
+  if (sh_total > kMaxPlanPositions) {  // more work positions than an int32 holds: refuse the plan
+    if (tid == 0) {
+      plan_refuse(sched);
+      atomicCAS(&g_mla_error, 0, MLA_ERR_INVALID_ARG);
+    }
+    return;
+  }
   const int64_t total = sh_total, Bq = plan_budget(total, U);
   plan_phase_units(seqlens, s_q, causal, NQB, pos, total, Bq, U, units, tid, nt);
   plan_phase_splits(seqlens, s_q, causal, NQB, pos, Bq, num_splits, tid, nt);
@@ -49,6 +59,9 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const int32_t* sched, 
                                                           const float* o_acc, const float* lse_acc, void* out,
                                                           float* lse, int out_f32) {
   pdl_wait_prerequisites();  // the decode kernel before it in the stream has finished
+  // metadata for other params, or a refused plan: nothing to merge (the decode kernel has
+  // reported it in the device error word)
+  if (sched[0] != kSchedMagic || sched[1] != U || sched[2] != NQB) return;
   const int qb = blockIdx.x, h0 = blockIdx.y * kCombineHeads, quarter = blockIdx.z;
   const int32_t* num_splits = sched + kSchedHeader + kUnitInts * U;
   const int32_t* split_offset = num_splits + NQB;
@@ -287,6 +300,87 @@ int32_t encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void*
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
 }
 
+// Tensor maps of recent calls.  A decode step calls the library once per layer with the
+// same query buffers and, per layer, its own cache pool; encoding the four maps on the host
+// every call costs microseconds, so the last few sets are kept, keyed on everything the
+// maps encode (device, base pointers, extents, cache format).
+struct MapKey {
+  int dev;
+  const void* q_rope;
+  const void* kv;
+  int H, NQB, num_pages, kv_dtype;
+  bool operator==(const MapKey& o) const {
+    return dev == o.dev && q_rope == o.q_rope && kv == o.kv && H == o.H && NQB == o.NQB &&
+           num_pages == o.num_pages && kv_dtype == o.kv_dtype;
+  }
+};
+struct MapSet {
+  MapKey key;
+  bool valid = false;
+  CUtensorMap qr, kvc, kvr, kvs;
+};
+constexpr int kMapCache = 16;
+MapSet g_maps[kMapCache];
+int g_map_next = 0;
+
+int32_t encode_maps(const MapKey& k, MapSet* m) {
+  int32_t st;
+  {
+    const uint64_t d[3] = {64, (uint64_t)k.H, (uint64_t)k.NQB};
+    const uint64_t s[2] = {64 * 2, (uint64_t)k.H * 64 * 2};
+    const uint32_t bx[3] = {32, 128, 1};
+    if ((st = encode_map(&m->qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k.q_rope, d, s, bx, CU_TENSOR_MAP_SWIZZLE_64B)))
+      return st;
+  }
+  if (k.kv_dtype == MLA_KV_BF16) {
+    const uint64_t d[2] = {576, (uint64_t)k.num_pages * 64};
+    const uint64_t s[1] = {576 * 2};
+    const uint32_t bc[2] = {64, 64}, br[2] = {32, 64};
+    if ((st = encode_map(&m->kvc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k.kv, d, s, bc, CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+    if ((st = encode_map(&m->kvr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k.kv, d, s, br, CU_TENSOR_MAP_SWIZZLE_64B)))
+      return st;
+    m->kvs = m->kvr;  // unused
+  } else {  // FP8 rows of 656 bytes: 512 codes, 4 float32 scales, 64 bf16 RoPE
+    const uint64_t d[2] = {656, (uint64_t)k.num_pages * 64};
+    const uint64_t s[1] = {656};
+    const uint32_t bc[2] = {256, 64}, br[2] = {64, 64}, bs[2] = {16, 64};
+    if ((st = encode_map(&m->kvc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k.kv, d, s, bc, CU_TENSOR_MAP_SWIZZLE_NONE)))
+      return st;
+    if ((st = encode_map(&m->kvr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k.kv, d, s, br, CU_TENSOR_MAP_SWIZZLE_64B)))
+      return st;
+    if ((st = encode_map(&m->kvs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k.kv, d, s, bs, CU_TENSOR_MAP_SWIZZLE_NONE)))
+      return st;
+  }
+  m->key = k;
+  m->valid = true;
+  return MLA_OK;
+}
+
+// The maps for key k into args: from the cache, or encoded now (and cached).
+int32_t tensor_maps(const MapKey& k, DecodeArgs* a) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  const MapSet* hit = nullptr;
+  for (const MapSet& m : g_maps)
+    if (m.valid && m.key == k) {
+      hit = &m;
+      break;
+    }
+  if (!hit) {
+    MapSet fresh;
+    const int32_t st = encode_maps(k, &fresh);
+    if (st != MLA_OK) return st;
+    g_maps[g_map_next] = fresh;
+    hit = &g_maps[g_map_next];
+    g_map_next = (g_map_next + 1) % kMapCache;
+  }
+  a->map_qr = hit->qr;
+  a->map_kvc = hit->kvc;
+  a->map_kvr = hit->kvr;
+  a->map_kvs = hit->kvs;
+  return MLA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -328,8 +422,11 @@ int32_t mla_plan_host(const mla_decode_params* p, int32_t num_units, const int32
   int32_t st = check_params(p);
   if (st != MLA_OK) return st;
   if (num_units < 1 || !cache_seqlens || !sched) return MLA_ERR_INVALID_ARG;
-  plan_units(cache_seqlens, p->batch, p->s_q, p->causal != 0, num_units, static_cast<int32_t*>(sched));
-  return MLA_OK;
+  for (int b = 0; b < p->batch; ++b)
+    if (cache_seqlens[b] < 0) return MLA_ERR_INVALID_ARG;
+  return plan_units(cache_seqlens, p->batch, p->s_q, p->causal != 0, num_units, static_cast<int32_t*>(sched))
+             ? MLA_OK
+             : MLA_ERR_INVALID_ARG;
 }
 
 int32_t mla_get_scheduler_metadata(const mla_decode_params* p, const int32_t* cache_seqlens, void* sched,
@@ -363,33 +460,10 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
   DecodeArgs a;
   std::memset(&a, 0, sizeof a);
   {
-    const uint64_t d[3] = {64, (uint64_t)H, (uint64_t)NQB};
-    const uint64_t s[2] = {64 * 2, (uint64_t)H * 64 * 2};
-    const uint32_t bx[3] = {32, 128, 1};
-    if ((st = encode_map(&a.map_qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_rope, d, s, bx, CU_TENSOR_MAP_SWIZZLE_64B)))
-      return st;
-  }
-  if (p->kv_dtype == MLA_KV_BF16) {
-    const uint64_t d[2] = {576, (uint64_t)p->num_pages * 64};
-    const uint64_t s[1] = {576 * 2};
-    const uint32_t bc[2] = {64, 64}, br[2] = {32, 64};
-    if ((st = encode_map(&a.map_kvc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_pages, d, s, bc,
-                         CU_TENSOR_MAP_SWIZZLE_128B)))
-      return st;
-    if ((st = encode_map(&a.map_kvr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_pages, d, s, br,
-                         CU_TENSOR_MAP_SWIZZLE_64B)))
-      return st;
-    a.map_kvs = a.map_kvr;  // unused
-  } else {  // FP8 rows of 656 bytes: 512 codes, 4 float32 scales, 64 bf16 RoPE
-    const uint64_t d[2] = {656, (uint64_t)p->num_pages * 64};
-    const uint64_t s[1] = {656};
-    const uint32_t bc[2] = {256, 64}, br[2] = {64, 64}, bs[2] = {16, 64};
-    if ((st = encode_map(&a.map_kvc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_pages, d, s, bc, CU_TENSOR_MAP_SWIZZLE_NONE)))
-      return st;
-    if ((st = encode_map(&a.map_kvr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_pages, d, s, br, CU_TENSOR_MAP_SWIZZLE_64B)))
-      return st;
-    if ((st = encode_map(&a.map_kvs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kv_pages, d, s, bs, CU_TENSOR_MAP_SWIZZLE_NONE)))
-      return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+    const MapKey key{dev, q_rope, kv_pages, H, NQB, p->num_pages, p->kv_dtype};
+    if ((st = tensor_maps(key, &a)) != MLA_OK) return st;
   }
   a.kv_fp8 = p->kv_dtype == MLA_KV_FP8_E4M3;
   a.q_nope = q_nope_absorbed;

@@ -33,10 +33,12 @@ constexpr int kTile = 64;                     // tokens per work tile (one page)
 #endif
 constexpr int kPieceFixedCost = MLA_PIECE_COST;
 
+// Keys query token t of a sequence of length L sees.  A negative length (outside the
+// contract; the scheduler kernel reports it) sees none.
 MLA_HD inline int32_t visible_keys(int32_t L, int s_q, int t, int causal) {
   int32_t n = causal ? L - s_q + 1 + t : L;
-  if (n < 0) n = 0;
   if (n > L) n = L;
+  if (n < 0) n = 0;
   return n;
 }
 
@@ -63,7 +65,11 @@ MLA_HD inline void plan_phase_cost(const int32_t* seqlens, int s_q, int causal, 
   }
 }
 
+// Largest total of cost positions a plan may have: positions are stored as int32.
+constexpr int64_t kMaxPlanPositions = 0x7FFFFFFF;
+
 // Phase 2 (one thread): exclusive prefix sum of cost -> pos (in place); returns the total.
+// A total above kMaxPlanPositions leaves pos unusable: the callers then refuse the plan.
 MLA_HD inline int64_t plan_phase_scan(int32_t* cost_to_pos, int NQB) {
   int64_t acc = 0;
   for (int qb = 0; qb < NQB; ++qb) {
@@ -155,19 +161,32 @@ MLA_HD inline void plan_phase_finish(int NQB, int U, int64_t B, int32_t* sched) 
   sched[5] = sched[6] = sched[7] = 0;
 }
 
+// A refused plan: a header without the magic word, which the decode and combine kernels
+// recognise as invalid metadata (they then write nothing).
+MLA_HD inline void plan_refuse(int32_t* sched) {
+  for (int i = 0; i < kSchedHeader; ++i) sched[i] = 0;
+}
+
 // Host twin: all phases in order, one "thread".  The split_offset region of
 // sched serves as scratch for the block positions until phase 5 fills it.
-MLA_HD inline void plan_units(const int32_t* seqlens, int B_, int s_q, int causal, int U, int32_t* sched) {
+// Returns false (and writes a refused header) when the lengths need more cost
+// positions than an int32 holds.
+MLA_HD inline bool plan_units(const int32_t* seqlens, int B_, int s_q, int causal, int U, int32_t* sched) {
   const int NQB = B_ * s_q;
   int32_t* units = sched + kSchedHeader;
   int32_t* num_splits = units + kUnitInts * U;
   int32_t* pos = num_splits + NQB;
   plan_phase_cost(seqlens, s_q, causal, NQB, pos, 0, 1);
   const int64_t total = plan_phase_scan(pos, NQB);
+  if (total > kMaxPlanPositions) {
+    plan_refuse(sched);
+    return false;
+  }
   const int64_t B = plan_budget(total, U);
   plan_phase_units(seqlens, s_q, causal, NQB, pos, total, B, U, units, 0, 1);
   plan_phase_splits(seqlens, s_q, causal, NQB, pos, B, num_splits, 0, 1);
   plan_phase_finish(NQB, U, B, sched);
+  return true;
 }
 
 }  // namespace mla

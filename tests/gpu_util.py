@@ -52,25 +52,33 @@ def half_ulp_bf16(x):
     return np.ldexp(1.0, (np.floor(np.log2(a)) - 8).astype(np.int64))
 
 
-def compare(out, lse, ref_out, ref_lse, tol, what="", out_bf16=False):
+def compare(out, lse, ref_out, ref_lse, tol, what="", out_bf16=False, raw=False):
     """Element-wise comparison against the oracle; returns the measured errors.
 
-    With out_bf16 the output tensor holds bf16 numbers, and storing the exact result
-    already costs up to half a bf16 ulp; the max-abs bound then applies to the error
-    beyond that: |out - ref| - half_ulp(ref) <= tol."""
+    max_abs_raw is max |out - ref| itself.  With out_bf16 the output tensor holds bf16
+    numbers, and storing the exact result already costs up to half a bf16 ulp (up to
+    0.0078 for |out| in [2, 4)); the max-abs bound then applies to the error beyond that,
+    |out - ref| - half_ulp(ref) (max_abs).  raw=True bounds max_abs_raw as well: on the
+    benchmark workloads |out| is far below 1, where half an ulp is tiny, so the literal
+    bound is affordable there."""
     fin = np.isfinite(ref_lse)
     assert np.array_equal(fin, np.isfinite(lse)), f"{what}: -inf pattern of lse differs"
     assert np.all(out[~fin] == 0), f"{what}: tokens with no visible key must give out = 0"
     diff = out - ref_out
     excess = np.abs(diff) - (half_ulp_bf16(ref_out) if out_bf16 else 0.0)
     max_abs = float(excess.max()) if diff.size else 0.0
+    max_abs_raw = float(np.abs(diff).max()) if diff.size else 0.0
     denom = float(np.linalg.norm(ref_out))
     rel_l2 = float(np.linalg.norm(diff) / denom) if denom > 0 else float(np.linalg.norm(diff))
     lse_err = float(np.abs(lse[fin] - ref_lse[fin]).max()) if fin.any() else 0.0
-    errs = dict(max_abs=max_abs, rel_l2=rel_l2, lse=lse_err)
+    errs = dict(max_abs=max_abs, max_abs_raw=max_abs_raw, rel_l2=rel_l2, lse=lse_err)
+    print(f"[parity] {what}: max_abs_raw={max_abs_raw:.3g} max_abs_beyond_bf16_rounding={max_abs:.3g} "
+          f"rel_l2={rel_l2:.3g} lse={lse_err:.3g}")
     assert np.all(np.isfinite(out)), f"{what}: non-finite output"
     if tol.get("max_abs") is not None:
         assert max_abs <= tol["max_abs"], f"{what}: max abs {max_abs:.3g} > {tol['max_abs']} ({errs})"
+        if raw:
+            assert max_abs_raw <= tol["max_abs"], f"{what}: raw max abs {max_abs_raw:.3g} > {tol['max_abs']} ({errs})"
     assert rel_l2 <= tol["rel_l2"], f"{what}: rel L2 {rel_l2:.3g} > {tol['rel_l2']} ({errs})"
     if tol.get("lse") is not None:
         assert lse_err <= tol["lse"], f"{what}: lse err {lse_err:.3g} > {tol['lse']} ({errs})"

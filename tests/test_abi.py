@@ -195,3 +195,24 @@ def test_non_positive_scale_is_rejected_before_any_launch(lib):
     for scale in (0.0, -0.07, float("nan"), float("inf")):
         st = lib.mla_decode_splitkv(ctypes.byref(p), buf, buf, buf, buf, buf, scale, buf, buf, buf, buf, None)
         assert st == 1, scale
+
+
+def test_plan_refuses_negative_lengths(lib):
+    """A negative length is outside the contract: the host twin refuses it."""
+    p = MlaDecodeParams.make(3, 1, 128, 10, 5, num_units=2)
+    with pytest.raises(_lib.MlaError):
+        _lib.mla_plan_host(p, 2, np.array([100, -1, 7], np.int32))
+
+
+def test_plan_refuses_more_positions_than_an_int32_holds(lib):
+    """Work positions are int32: lengths that need more than 2^31 - 1 of them in total are refused
+    (and the metadata header loses its magic word, so no kernel would use it), where a smaller
+    total of the same shape still plans."""
+    B = 1 << 17
+    p = MlaDecodeParams.make(B, 1, 128, 1 << 20, 1 << 14, num_units=76)
+    over = np.full(B, 1 << 20, np.int32)                 # 16384 tiles + 6 each: 2^17 * 16390 > 2^31
+    with pytest.raises(_lib.MlaError):
+        _lib.mla_plan_host(p, 76, over)
+    ok = np.full(B, 1 << 19, np.int32)                   # 8192 tiles + 6 each: below 2^31
+    sched = _lib.mla_plan_host(p, 76, ok)
+    assert sched[0] == _lib.SCHED_MAGIC and sched[1] == 76 and sched[2] == B

@@ -36,7 +36,9 @@ def full_check(w, tol=BF16_TOL, num_units=0, what=""):
 
 def test_workload_tiny_full():
     w = mw.make_workload(0)
-    errs = full_check(w)
+    out, lse, _ = run_gpu(w)
+    ref_out, ref_lse = oracle_full(w, threads=THREADS)
+    errs = compare(out, lse, ref_out, ref_lse, BF16_TOL, w.name, raw=True)
     print("tiny", errs)
 
 
@@ -48,7 +50,8 @@ def test_workload_full_size_sampled(index):
     items = []
     for b in range(w.batch):
         for t in range(w.s_q):
-            heads = sorted(rng.choice(w.num_heads, size=3, replace=False).tolist())
+            # one head from each 32-row group (a warp's tensor-memory lanes) of every (sequence, token)
+            heads = [int(g + rng.integers(0, 32)) for g in range(0, w.num_heads, 32)]
             items.append((b, t, heads))
     ref = oracle_sampled(w, items, threads=THREADS)
     got_o, got_l, ref_o, ref_l = [], [], [], []
@@ -58,7 +61,7 @@ def test_workload_full_size_sampled(index):
         ref_o.append(o)
         ref_l.append(l)
     errs = compare(np.concatenate(got_o), np.concatenate(got_l), np.concatenate(ref_o), np.concatenate(ref_l),
-                   FP8_TOL if w.kv_dtype == "fp8" else BF16_TOL, w.name, out_bf16=True)
+                   FP8_TOL if w.kv_dtype == "fp8" else BF16_TOL, w.name, out_bf16=True, raw=True)
     print(w.name, errs)
 
 
@@ -126,6 +129,29 @@ def test_length_beyond_the_block_table_is_reported():
     assert mla_device_error(clear=True) == MLA_ERR_INVALID_ARG
     compare(out[:1].float().cpu().numpy().astype(np.float64), lse[:1].cpu().numpy().astype(np.float64),
             ref_out[:1], ref_lse[:1], BF16_TOL, "valid sequence next to an overlong one", out_bf16=True)
+
+
+def test_negative_length_is_reported_and_decoded_as_empty():
+    """A negative length breaks the call's contract: the scheduler reports MLA_ERR_INVALID_ARG in
+    the device error word and plans the sequence as empty (out = 0, lse = -inf); the other
+    sequences' results are still right."""
+    import torch
+    from mla_absorbed_decode_02_gb300 import Decoder, MLA_ERR_INVALID_ARG, mla_device_error
+    w = mw.make_custom([100, 64, 3000], num_heads=128, seed=26)
+    ref_out, ref_lse = oracle_full(w)
+    q_nope, q_rope, kv, bt, seq = to_device(w)
+    seq[1] = -5
+    dec = Decoder(params_for(w, num_units=3))
+    dec.plan(seq)
+    out, lse = dec.decode(q_nope, q_rope, kv, bt, seq, w.scale)
+    torch.cuda.synchronize()
+    assert mla_device_error(clear=True) == MLA_ERR_INVALID_ARG
+    o = out.float().cpu().numpy().astype(np.float64)
+    l = lse.cpu().numpy().astype(np.float64)
+    assert np.all(o[1] == 0) and np.all(l[1] == -np.inf)
+    keep = [0, 2]
+    compare(o[keep], l[keep], ref_out[keep], ref_lse[keep], BF16_TOL, "valid sequences next to a negative length",
+            out_bf16=True)
 
 
 def test_all_pages_alias_one_physical_page():

@@ -332,3 +332,61 @@ def test_threads_match_single_thread():
     a = P.full(threads=1)
     b = P.full(threads=3)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---------------------------------------------------------------- the Python marshalling helpers
+
+def test_bf16_widening_all_patterns():
+    """oracle.bf16_bits_to_f64 on every one of the 65,536 bf16 bit patterns, against torch's own
+    bf16 -> float64 conversion and against the format's definition (sign, 8-bit exponent with bias
+    127, 7-bit fraction; exponent 0 = subnormal, 255 = inf / NaN)."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):          # numpy flags the signalling-NaN patterns as it widens them
+        got = oracle.bf16_bits_to_f64(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert nan.sum() == 2 * 127                                   # exponent 255, fraction != 0, both signs
+    assert np.array_equal(got[~nan].view(np.uint64), ref[~nan].view(np.uint64))   # bit for bit, -0.0 included
+    sign = np.where(bits >> 15, -1.0, 1.0)
+    e = ((bits >> 7) & 0xFF).astype(np.int64)
+    f = (bits & 0x7F).astype(np.float64)
+    defn = np.where(e == 0, sign * f * 2.0 ** -133, sign * (1.0 + f / 128.0) * np.ldexp(1.0, e - 127))
+    fin = e < 255
+    assert np.array_equal(got[fin], defn[fin])
+    assert np.all(np.isinf(got[(e == 255) & (f == 0)]))
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_from_workload_matches_a_problem_built_by_hand(kv_dtype):
+    """oracle.from_workload: which array is the absorbed query and which the RoPE query, the cache
+    kind, the causal flag, the scale and the page size of a workload all reach the oracle.  The
+    hand-built problem widens the queries with torch and, for the FP8 cache, dequantises the codes
+    with torch's E4M3 type times the stored float32 tile scale; the results must agree bit for bit.
+    Two new tokens, not causal: a dropped causal flag would change the first token's keys."""
+    import mla_workloads as mw
+    w = mw.make_custom([70, 129, 3], num_heads=4, s_q=2, causal=False, kv_dtype=kv_dtype, seed=61)
+    P = oracle.from_workload(w)
+    widen = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert P.q_nope.shape == (3, 2, 4, 512) and P.q_rope.shape == (3, 2, 4, 64)
+    assert np.array_equal(P.q_nope, widen(w.q_nope)) and np.array_equal(P.q_rope, widen(w.q_rope))
+    assert P.causal is False and P.scale == 1 / math.sqrt(192) and P.page_size == 64
+    assert np.array_equal(P.block_table, w.block_table) and np.array_equal(P.seqlens, w.seqlens)
+    if kv_dtype == "bf16":
+        assert P.kv_kind == KV_BF16
+        pool = widen(w.kv)
+    else:
+        assert P.kv_kind == KV_FP8
+        rows = w.kv.reshape(-1, mw.FP8_ROW_BYTES)
+        codes = torch.from_numpy(rows[:, :512].copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        scales = rows[:, 512:528].copy().view(np.float32).astype(np.float64)
+        rope = widen(rows[:, 528:].copy().view(np.uint16))
+        pool = np.concatenate([codes * np.repeat(scales, 128, axis=1), rope], axis=1).reshape(w.kv.shape[0], 64, 576)
+    hand = Problem(widen(w.q_nope), widen(w.q_rope), pool, KV_F64, w.block_table, w.seqlens, 1 / math.sqrt(192),
+                   causal=False, page_size=64)
+    a, b = P.full(), hand.full()
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    # and the flag matters here: the causal reading of the same inputs differs
+    c = Problem(widen(w.q_nope), widen(w.q_rope), pool, KV_F64, w.block_table, w.seqlens, 1 / math.sqrt(192),
+                causal=True, page_size=64).full()
+    assert not np.array_equal(a[1][:, 0], c[1][:, 0])
