@@ -429,7 +429,8 @@ def run_ours(args, w, peaks, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8-e4m3 cache, bf16 mma",
         "data": "synthetic (seeded N(0,1) bf16 queries and cache, random page permutation)",
-        "config": {"workload": args.workload, "batch": w.batch, "heads": w.num_heads, "s_q": w.s_q,
+        "config": {"workload": args.workload + (f" (first {w.batch} sequences)" if args.batch else ""),
+                   "batch": w.batch, "heads": w.num_heads, "s_q": w.s_q,
                    "seqlens": f"{int(w.seqlens.min())}..{int(w.seqlens.max())} (sum {int(w.seqlens.sum())})",
                    "kv_dtype": w.kv_dtype, "pages": w.num_pages, "units": units,
                    "l2": "flushed before every step (256 MiB write)", "parallelism": f"replicas x{n}",
@@ -479,12 +480,16 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="time the chosen workload only")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="keep only the first B sequences of the workload (same recipe; for profiling small cases)")
     args = ap.parse_args()
     import mla_workloads as mw
 
     world, rank, local = dist_env()
     peaks = load_peaks()
     w = mw.make_workload(WORKLOAD_INDEX[args.workload])
+    if args.batch:
+        w = mw.first_sequences(w, args.batch)
     threads = os.cpu_count() or 1
 
     if args.impl == "reference":

@@ -13,7 +13,7 @@
 // the A operand in tensor memory, the RoPE-query half in shared memory), and
 // the two CTAs swap partial scores through distributed shared memory
 // (st.async), encoded as 16-bit block floating point -- one shared exponent per
-// (head, 32-token chunk), 16-bit signed mantissas.  Each CTA adds the peer's
+// (head, tile), 15-bit magnitudes with sign.  Each CTA adds the peer's
 // rounded half to its own exact half, runs the online softmax for its output
 // half, writes P (bf16) to shared memory, and accumulates O_half += P V_half
 // (tcgen05.mma, N = 256, V read MN-major from the same shared-memory page the
@@ -34,7 +34,7 @@
 // (only when a tile's max exceeds it by more than 8 in log2 units), and O is
 // rescaled only then.
 //
-// Pipelining.  Four 36 KB shared-memory stages (a page stays resident from its
+// Pipelining.  Five 36 KB shared-memory stages (a page stays resident from its
 // load through QK, softmax and PV, because the latent is key and value at
 // once).  QK and PV are issued by two different warps, so the scores of the
 // next tiles never wait for the P of the current one.
@@ -181,10 +181,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Exponent e (clamped) with |x| < 2^e for the largest |x| of a chunk; the
-// 16-bit mantissa of x is then rint(x * 2^(15-e)).
+// Exponent e (clamped) of a row's block: every |x| of the row is below 2^e (1 - 2^-16)
+// (e is the exponent bucket of amax * (1 + 2^-15), one rounding included), so
+// rint(x * 2^(14-e)) lies in [-(2^14 - 1), 2^14 - 1].
 __device__ __forceinline__ int bfp_exponent(float amax) {
-  int e = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 126;
+  const float a = fmaf(amax, 3.0517578125e-05f, amax);  // amax * (1 + 2^-15)
+  int e = (int)((__float_as_uint(a) >> 23) & 0xFF) - 126;
   e = e < -60 ? -60 : e;
   e = e > 110 ? 110 : e;
   return e;
@@ -235,25 +237,26 @@ __device__ __forceinline__ void mask_pairs(uint64_t (&sc)[32], int valid, float 
   }
 }
 
-// Block floating point without conversion instructions, one exponent e per row
-// and tile (|x| < 2^e for every partial score x of the row).  Encode: n =
-// rint(x * 2^(14-e)) lies in [-2^14, 2^14]; adding 1.5 * 2^23 + 2^15 in one FMA
-// leaves n + 2^15 (offset binary) in the low 16 bits of the float, and two such
-// halves are packed into one word.  Decode: the half u placed in the mantissa of
-// 2^23 gives the float 2^23 + u = 2^23 + 2^15 + n, exactly; the receiver folds it
-// into its own partial with one FMA by kp = 2^(e_peer - 14), which leaves the
-// constant bias beta = (2^23 + 2^15) kp on every score of the row -- the softmax
-// only ever sees scores relative to the row max, so beta is removed there.
-constexpr float kBfpMagic = 12615680.0f;  // 1.5 * 2^23 + 2^15
-constexpr float kBfpBias = 8421376.0f;    // 2^23 + 2^15
+// Block floating point without conversion instructions, one exponent e per row and
+// tile.  Encode: n = rint(x * 2^(14-e)) lies in [-(2^14 - 1), 2^14 - 1]; adding
+// 1.5 * 2^23 + 3 * 2^14 in one FMA leaves u = n + 3 * 2^14, which lies in [2^15, 2^16),
+// in the low 16 bits of the float, and two such halves are packed into one word.
+// Decode: u placed at bits 8..23 under the exponent of 0.5 gives the float
+// 1 + (u - 2^15) 2^-15 = 1.5 + n 2^-15 exactly (u >= 2^15 sets the exponent's low bit,
+// so every u lands in [1, 2)); the receiver folds it into its own partial with one
+// FMA by 2^(e_peer + 1), which leaves the constant bias beta = 3 * 2^e_peer on every
+// score of the row -- the softmax only ever sees scores relative to the row max, so
+// beta is removed there.  The peer's half is off by at most half a quantum,
+// 2^(e_peer - 15); the biased sum, below 2^(e_peer + 3), rounds within 2^(e_peer - 21).
+constexpr float kBfpMagic = 12632064.0f;  // 1.5 * 2^23 + 3 * 2^14
 __device__ __forceinline__ uint32_t bfp_pack_pair(uint64_t xy, uint64_t k) {
   float a, b;
   unpack_f32x2(ffma_f32x2(xy, k, splat_f32x2(kBfpMagic)), a, b);
   return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x5410);
 }
-// The two halves of w as the floats 2^23 + u.
+// The two halves u of w as the floats 1 + (u - 2^15) 2^-15 (u at bits 8..23 of 0x3F000000).
 __device__ __forceinline__ uint64_t bfp_unpack_pair(uint32_t w) {
-  return pack_b32x2(__byte_perm(w, 0x4B000000u, 0x7410), __byte_perm(w, 0x4B000000u, 0x7432));
+  return pack_b32x2(__byte_perm(w, 0x3F000000u, 0x7104), __byte_perm(w, 0x3F000000u, 0x7324));
 }
 
 __device__ __forceinline__ void st_async_b32(uint32_t cluster_dst, uint32_t v, uint32_t cluster_bar) {
@@ -820,7 +823,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           }
           const int valid = x.valid;
           if (kFull && valid < kTileTok) mask_pairs(sc, valid, 0.f);  // columns past the sequence end: sent as 0
-          // ---- encode (16-bit block floating point, one exponent per 32 columns) and send
+          // ---- encode (16-bit block floating point, one exponent per row and tile) and send
           {
             float a[4] = {0.f, 0.f, 0.f, 0.f};
   #pragma unroll
@@ -832,14 +835,12 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
             }
             const int e = bfp_exponent(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])));
             const uint64_t k = splat_f32x2(pow2f(14 - e));
-            uint32_t pk[32];
-  #pragma unroll
-            for (int u = 0; u < 32; ++u) pk[u] = bfp_pack_pair(sc[u], k);
             if (!(ok = wait_warp(bar(B_X_FREE + sb), ph ^ 1, wc, kSiteXFree))) return false;
             const uint32_t full = peer_bar0 + 8 * (B_X_FULL + sb);
   #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              st_async_v4(peer_x + (j * kRows + r) * 16, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3], full);
+            for (int j = 0; j < 8; ++j)  // each 16-byte chunk goes out as soon as it is encoded
+              st_async_v4(peer_x + (j * kRows + r) * 16, bfp_pack_pair(sc[4 * j], k), bfp_pack_pair(sc[4 * j + 1], k),
+                          bfp_pack_pair(sc[4 * j + 2], k), bfp_pack_pair(sc[4 * j + 3], k), full);
             st_async_b32(peer_xe + r * 4, (uint32_t)e, full);
           }
           // ---- the peer's half of the same scores
@@ -849,9 +850,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
             uint32_t pe;
             asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pe) : "r"(my_xe + r * 4));
             slot_dep = pe;
-            const float kpf = pow2f((int)pe - 14);
+            const float kpf = pow2f((int)pe + 1);
             const uint64_t kp = splat_f32x2(kpf);
-            beta = kBfpBias * kpf;  // exact: a power of two times a 24-bit integer
+            beta = 1.5f * kpf;  // exact
   #pragma unroll
             for (int j = 0; j < 8; ++j) {
               uint32_t wv[4];

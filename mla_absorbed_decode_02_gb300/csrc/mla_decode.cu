@@ -50,11 +50,15 @@ __global__ void __launch_bounds__(1024) mla_sched_kernel(const int32_t* seqlens,
 // out = sum_i exp(lse_i - lse) * out_i, lse = M + ln sum_i exp(lse_i - M), M = max_i lse_i
 // (the merge of split-KV partial results, "MLA inference: two computation paths and
 // FlashMLA", section "Decode attention becomes a compute problem").  Query blocks that see
-// no key get out = 0, lse = -inf.  One CTA of 256 threads per (query block, 16 heads, 128
-// output columns): the 16 combined LSEs first (two heads per warp, the splits spread over
-// 16 lanes), then every thread streams 2 float4 columns of one head per split, four splits'
-// loads in flight together (a query block split across many units is merged by many CTAs).
-constexpr int kCombineHeads = 16, kCombineQuarters = 4;
+// no key get out = 0, lse = -inf.  One CTA of 256 threads per (query block, 16 heads, one
+// of Z column slices): the 16 combined LSEs first (two heads per warp, the splits spread
+// over 16 lanes), then 16 threads per head stream the slice's float4 columns of every
+// split, kNf columns each, the splits dealt round-robin over kG adjacent lanes (summed by
+// shuffles at the end), four of a lane's splits in flight together.  The host picks Z (and
+// with it kG, kNf) from the splits per query block it expects: long sequences split over
+// many units are merged by many more CTAs.
+constexpr int kCombineHeads = 16;
+template <int kG, int kNf>
 __global__ void __launch_bounds__(256) mla_combine_kernel(const int32_t* sched, int U, int NQB, int H,
                                                           const float* o_acc, const float* lse_acc, void* out,
                                                           float* lse, int out_f32) {
@@ -62,7 +66,8 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const int32_t* sched, 
   // metadata for other params, or a refused plan: nothing to merge (the decode kernel has
   // reported it in the device error word)
   if (sched[0] != kSchedMagic || sched[1] != U || sched[2] != NQB) return;
-  const int qb = blockIdx.x, h0 = blockIdx.y * kCombineHeads, quarter = blockIdx.z;
+  constexpr int kW = kNf * 16 / kG;  // float4 columns of a slice (of 128 per head)
+  const int qb = blockIdx.x, h0 = blockIdx.y * kCombineHeads, slice = blockIdx.z;
   const int32_t* num_splits = sched + kSchedHeader + kUnitInts * U;
   const int32_t* split_offset = num_splits + NQB;
   const int ns = num_splits[qb];
@@ -84,55 +89,65 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const int32_t* sched, 
     if (sub == 0) s_lse[hh] = M > -INFINITY ? M + logf(S) : -INFINITY;
   }
   __syncthreads();
-  const int hh = tid >> 4, h = h0 + hh, c = 32 * quarter + (tid & 15);  // float4 columns c, c + 16
-  if (h >= H) return;
+  const int hh = tid >> 4, h = h0 + hh, sub = tid & 15, g = sub % kG, ci = sub / kG;
   const float L = s_lse[hh];
   const int64_t split_stride = (int64_t)H * 128;  // float4 per split
-  const float4* src = reinterpret_cast<const float4*>(o_acc) + ((int64_t)off * H + h) * 128 + c;
-  const float* lsrc = lse_acc + (int64_t)off * H + h;
-  float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-  auto add = [&](float wgt, const float4& v, float4& a) {
-    a.x += wgt * v.x;
-    a.y += wgt * v.y;
-    a.z += wgt * v.z;
-    a.w += wgt * v.w;
-  };
-  int i = 0;
-  for (; i + 4 <= ns; i += 4) {
-    float4 v[4][2];
-    float lw[4];
+  const int c0 = kW * slice + ci;                 // first float4 column; then every 16 / kG
+  const float4* src = reinterpret_cast<const float4*>(o_acc) + ((int64_t)off * H + (h < H ? h : 0)) * 128 + c0;
+  const float* lsrc = lse_acc + (int64_t)off * H + (h < H ? h : 0);
+  float4 acc[kNf];
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      lw[s] = lsrc[(int64_t)(i + s) * H];
-      v[s][0] = __ldcs(src + (i + s) * split_stride);
-      v[s][1] = __ldcs(src + (i + s) * split_stride + 16);
-    }
+  for (int f = 0; f < kNf; ++f) acc[f] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (h < H) {
+    for (int i0 = g; i0 < ns; i0 += 4 * kG) {
+      float4 v[4][kNf];
+      float wgt[4];
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const float wgt = expf(lw[s] - L);
-      add(wgt, v[s][0], acc[0]);
-      add(wgt, v[s][1], acc[1]);
+      for (int k = 0; k < 4; ++k) {
+        const int i = i0 + k * kG;
+        const bool in = i < ns;
+        wgt[k] = in ? lsrc[(int64_t)i * H] : -INFINITY;
+#pragma unroll
+        for (int f = 0; f < kNf; ++f)
+          v[k][f] = in ? __ldcs(src + i * split_stride + f * (16 / kG)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float wk = expf(wgt[k] - L);
+#pragma unroll
+        for (int f = 0; f < kNf; ++f) {
+          acc[f].x += wk * v[k][f].x;
+          acc[f].y += wk * v[k][f].y;
+          acc[f].z += wk * v[k][f].z;
+          acc[f].w += wk * v[k][f].w;
+        }
+      }
     }
   }
-  for (; i < ns; ++i) {
-    const float wgt = expf(lsrc[(int64_t)i * H] - L);
-    add(wgt, __ldcs(src + i * split_stride), acc[0]);
-    add(wgt, __ldcs(src + i * split_stride + 16), acc[1]);
-  }
+#pragma unroll
+  for (int o = 1; o < kG; o <<= 1)
+#pragma unroll
+    for (int f = 0; f < kNf; ++f) {
+      acc[f].x += __shfl_xor_sync(0xffffffffu, acc[f].x, o);
+      acc[f].y += __shfl_xor_sync(0xffffffffu, acc[f].y, o);
+      acc[f].z += __shfl_xor_sync(0xffffffffu, acc[f].z, o);
+      acc[f].w += __shfl_xor_sync(0xffffffffu, acc[f].w, o);
+    }
+  if (h >= H || g != 0) return;
   const int64_t row = (int64_t)qb * H + h;
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int d = 4 * (c + 16 * k);
+  for (int f = 0; f < kNf; ++f) {
+    const int d = 4 * (c0 + f * (16 / kG));
     if (out_f32) {
-      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + row * 512 + d) = acc[k];
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + row * 512 + d) = acc[f];
     } else {
       uint2 o;
-      o.x = pack_bf16(acc[k].x, acc[k].y);
-      o.y = pack_bf16(acc[k].z, acc[k].w);
+      o.x = pack_bf16(acc[f].x, acc[f].y);
+      o.y = pack_bf16(acc[f].z, acc[f].w);
       *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + row * 512 + d) = o;
     }
   }
-  if ((tid & 15) == 0 && quarter == 0) lse[row] = L;
+  if (ci == 0 && slice == 0) lse[row] = L;
 }
 
 // ----------------------------------------------------------------- FP8 cache writer
@@ -517,10 +532,14 @@ int32_t mla_combine(const mla_decode_params* p, void* out, float* lse, const voi
   const float* o_acc = static_cast<const float*>(workspace);
   const float* lse_acc =
       reinterpret_cast<const float*>(static_cast<const char*>(workspace) + align256(slots * H * 512 * sizeof(float)));
+  // Column slices per (query block, 16 heads): enough CTAs for the splits a query block is
+  // expected to have when the units are spread over the query blocks (1 + U / NQB).
+  const int expect = 1 + (U + NQB - 1) / NQB;
+  const int Z = expect <= 4 ? 4 : expect <= 8 ? 8 : expect <= 16 ? 16 : 32;
   // programmatic dependent launch: this grid is set up while the decode kernel before it
   // drains, and waits (griddepcontrol.wait) for it before reading the partials
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(NQB, (H + kCombineHeads - 1) / kCombineHeads, kCombineQuarters);
+  cfg.gridDim = dim3(NQB, (H + kCombineHeads - 1) / kCombineHeads, Z);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = static_cast<cudaStream_t>(stream);
@@ -529,10 +548,18 @@ int32_t mla_combine(const mla_decode_params* p, void* out, float* lse, const voi
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_combine_kernel, static_cast<const int32_t*>(sched), U, NQB, H, o_acc, lse_acc,
-                            out, lse, (int)(p->out_dtype == MLA_OUT_F32)) == cudaSuccess
-             ? MLA_OK
-             : MLA_ERR_CUDA;
+  const int32_t* sc = static_cast<const int32_t*>(sched);
+  const int of32 = (int)(p->out_dtype == MLA_OUT_F32);
+  cudaError_t e;
+  if (Z == 4)
+    e = cudaLaunchKernelEx(&cfg, mla_combine_kernel<1, 2>, sc, U, NQB, H, o_acc, lse_acc, out, lse, of32);
+  else if (Z == 8)
+    e = cudaLaunchKernelEx(&cfg, mla_combine_kernel<1, 1>, sc, U, NQB, H, o_acc, lse_acc, out, lse, of32);
+  else if (Z == 16)
+    e = cudaLaunchKernelEx(&cfg, mla_combine_kernel<2, 1>, sc, U, NQB, H, o_acc, lse_acc, out, lse, of32);
+  else
+    e = cudaLaunchKernelEx(&cfg, mla_combine_kernel<4, 1>, sc, U, NQB, H, o_acc, lse_acc, out, lse, of32);
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 int32_t mla_decode(const mla_decode_params* p, const void* q_nope_absorbed, const void* q_rope, const void* kv_pages,

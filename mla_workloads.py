@@ -165,3 +165,12 @@ def make_workload(index: int, seed: int | None = None) -> Workload:
     w.meta["index"] = index
     w.meta["seed"] = seed
     return w
+
+
+def first_sequences(w: Workload, batch: int) -> Workload:
+    """The same workload cut to its first `batch` sequences (pages and cache pool unchanged)."""
+    import dataclasses
+    b = max(1, min(int(batch), w.batch))
+    return dataclasses.replace(w, batch=b, seqlens=w.seqlens[:b].copy(), block_table=w.block_table[:b].copy(),
+                               q_nope=w.q_nope[:b].copy(), q_rope=w.q_rope[:b].copy(),
+                               meta=dict(w.meta, first_sequences=b))

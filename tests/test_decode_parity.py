@@ -74,6 +74,15 @@ def test_ragged_lengths_and_splits(num_units):
     full_check(w, num_units=num_units, what=f"ragged U={num_units}")
 
 
+@pytest.mark.parametrize("num_units", [9, 20, 40, 76])
+def test_combine_column_slicings(num_units):
+    """Four long sequences over 9, 20, 40 and 76 units: the combine merges up to ~20 splits per
+    query block, with 4, 8, 16 or 32 column slices per (block, 16 heads) and the splits of a
+    column dealt over 1, 2 or 4 lanes."""
+    w = mw.make_custom([30000, 9000, 20000, 3000], num_heads=128, seed=27)
+    full_check(w, num_units=num_units, what=f"combine U={num_units}")
+
+
 @pytest.mark.parametrize("H", [1, 16, 17, 100, 128])
 def test_head_counts(H):
     w = mw.make_custom([130, 7, 700], num_heads=H, seed=12)
@@ -178,6 +187,66 @@ def test_dominant_key():
     big = np.sign(kr) * 8.0
     w.kv[page, 123 % 64, 512:] = mw.to_bf16_bits(big.astype(np.float32))
     full_check(w, num_units=2, what="dominant key")
+
+
+def _scaled_queries(w, factor):
+    """Queries multiplied by a power of two (exact in bf16)."""
+    widen = lambda b: (b.astype(np.uint32) << 16).view(np.float32)
+    w.q_nope[:] = mw.to_bf16_bits(widen(w.q_nope) * factor)
+    w.q_rope[:] = mw.to_bf16_bits(widen(w.q_rope) * factor)
+    return w
+
+
+def _exchange_bound(w):
+    """What the score exchange of a CTA pair may cost, from the inputs: each CTA of the pair holds a
+    partial score over 256 latent + 32 RoPE dims; the one it receives is rounded to a multiple of
+    2^(e-14), e the exponent bucket of the largest |partial| of its row and tile (times 1 + 2^-15),
+    so no score is off by more than 2^(e_max - 15) * scale and the LSE, which moves by at most the
+    largest score error, neither.  Returns (that bound in nats, the largest |c| of a visible key,
+    the widest spread of one row's scores)."""
+    widen = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    big, cmax, spread = 0.0, 0.0, 0.0
+    for b in range(w.batch):
+        L = int(w.seqlens[b])
+        if L == 0:
+            continue
+        rows = widen(np.concatenate([w.kv[w.block_table[b, i]] for i in range((L + 63) // 64)])[:L])
+        cmax = max(cmax, float(np.abs(rows[:, :512]).max()))
+        for t in range(w.s_q):
+            q = np.concatenate([widen(w.q_nope[b, t]), widen(w.q_rope[b, t])], axis=-1)   # [H, 576]
+            spread = max(spread, float(np.ptp(rows @ q.T * w.scale, axis=0).max()))
+            for h in (0, 1):
+                lat, rope = slice(256 * h, 256 * h + 256), slice(512 + 32 * h, 512 + 32 * h + 32)
+                part = rows[:, lat] @ q[:, lat].T + rows[:, rope] @ q[:, rope].T
+                big = max(big, float(np.abs(part).max()))
+    e_max = math.floor(math.log2(big * (1 + 2.0 ** -10))) + 1
+    return 2.0 ** (e_max - 15) * w.scale, cmax, spread
+
+
+@pytest.mark.parametrize("num_units", [0, 3, 7])
+def test_high_dynamic_range_logits(num_units):
+    """Queries scaled by 8: the scores of a row span more than 100 nats and one key usually
+    dominates.  The LSE must stay within what the 16-bit score exchange between the two CTAs of a
+    pair can cost (the bound computed from the inputs; about 2.3e-3 nats here), rel L2 within
+    5e-3, and max |out - ref| beyond bf16 rounding within 1e-2 plus what rounding P to bf16 for
+    the PV product can cost when one key carries all the weight (2^-9 of the largest |c|).
+    Ragged lengths, several unit counts (splits merged by the combine)."""
+    w = _scaled_queries(mw.make_custom([1, 63, 65, 700, 2049, 4100, 9000], num_heads=128, seed=71), 8.0)
+    bound, cmax, spread = _exchange_bound(w)
+    assert spread > 100.0
+    tol = dict(max_abs=1e-2 + cmax * 2.0 ** -9, rel_l2=5e-3, lse=bound * 1.01 + 2e-5)
+    full_check(w, tol=tol, num_units=num_units, what=f"high dynamic range x8 U={num_units}")
+
+
+@pytest.mark.parametrize("num_units", [0, 3, 7])
+def test_large_logits_within_the_stated_tolerance(num_units):
+    """Queries scaled by 4 (scores of a row spread over ~50 nats): the LSE within the stated 1e-3
+    and rel L2 within 5e-3, max |out - ref| beyond bf16 rounding within 1e-2 plus the bf16 P term."""
+    w = _scaled_queries(mw.make_custom([1, 63, 65, 700, 2049, 4100, 9000], num_heads=128, seed=71), 4.0)
+    bound, cmax, spread = _exchange_bound(w)
+    assert spread > 45.0 and bound < 1.2e-3
+    tol = dict(max_abs=1e-2 + cmax * 2.0 ** -9, rel_l2=5e-3, lse=1e-3)
+    full_check(w, tol=tol, num_units=num_units, what=f"large logits x4 U={num_units}")
 
 
 def test_long_tail_row_garbage_is_ignored():
