@@ -382,9 +382,17 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Everything above touches no global memory: it runs while the kernel before this one in the
-  // stream is still finishing (programmatic dependent launch).  Its writes (the metadata, the
-  // inputs) are visible from here on.
+  // The tensor maps are launch parameters, nothing the kernel before this one writes: their
+  // fetch overlaps that kernel's end too.
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&args.map_qr);
+    prefetch_tensormap(&args.map_kvc);
+    prefetch_tensormap(&args.map_kvr);
+    if (kFp8) prefetch_tensormap(&args.map_kvs);
+  }
+  // Everything above touches no other global memory: it runs while the kernel before this one
+  // in the stream is still finishing (programmatic dependent launch).  Its writes (the
+  // metadata, the inputs) are visible from here on.
   pdl_wait_prerequisites();
   // ---- unit record (uniform across the cluster); bail out early on bad metadata
   const int32_t* sched = args.sched;
@@ -418,49 +426,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
   if (warp == 0) {
     // ================================================================ TMA producer
     if (lane == 0) {
-      prefetch_tensormap(&args.map_qr);
-      prefetch_tensormap(&args.map_kvc);
-      prefetch_tensormap(&args.map_kvr);
-      if (kFp8) prefetch_tensormap(&args.map_kvs);
       const uint64_t pol_kv = l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
-      TileCursor cur;
-      cur.init(walker0);
-      TileInfo ti;
-      PieceWalker ahead = walker0;  // one piece ahead of the tile walk
-      Piece np;
-      ahead.next(np);  // piece 0
-      int next_qb = -1, prev_qb = -1, prev_split = 0;
-      uint32_t t = 0, piece_no = 0;
-      while (cur.next(ti)) {
-        if (ti.first) {
-          if (piece_no > 0 && !wait_one(bar(B_QR_EMPTY), (piece_no - 1) & 1, wc, kSiteQEmpty)) break;
-          mbar_arrive_expect_tx(bar(B_QR_FULL), 8192);
-          tma_load_3d(base + SM_QR, &args.map_qr, bar(B_QR_FULL), 32 * half, 0, ti.qb, pol_q);
-          ++piece_no;
-          next_qb = ahead.next(np) ? np.qb : -1;
-        }
-        const uint32_t st = t % kStages, ph = (t / kStages) & 1;
-        if (!wait_one(bar(B_KV_EMPTY + st), ph ^ 1, wc, kSiteKvEmpty)) break;
-        {  // the tile's schedule entry for the softmax warpgroups
-          const uint32_t e = base + SM_TI + (t % kTiRing) * 32;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(e), "r"(ti.qb), "r"(ti.valid), "r"(ti.split),
-                       "r"((ti.first ? 1 : 0) | (ti.last ? 2 : 0))
-                       : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(e + 16), "r"((int)piece_no - 1), "r"(next_qb),
-                       "r"(prev_qb), "r"(prev_split)
-                       : "memory");
-          mbar_arrive(bar(B_TI_FULL + (t % kTiRing)));
-          prev_qb = ti.qb;
-          prev_split = ti.split;
-        }
-        const int b = ti.qb / args.s_q;
-        int lp = ti.tile;  // logical page
-        if (lp >= args.max_pages) {  // a length beyond the block table: reported; no read past the row
-          atomicCAS(&g_mla_error, 0, 1);
-          lp = args.max_pages - 1;
-        }
-        const int page = args.block_table[(int64_t)b * args.max_pages + lp];
+      // one page into stage st: the half of its 64 rows this CTA owns
+      auto load_page = [&](uint32_t st, int page) {
         const uint32_t sbase = base + st * kStageBytes;
         if (kFp8) {  // 656-byte rows: codes of this half, its RoPE half, the 4 tile scales
           mbar_arrive_expect_tx(bar(B_KV_FULL + st), kFp8StageTx);
@@ -474,6 +443,55 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
                         pol_kv);
           tma_load_2d(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 512 + 32 * half, page * 64, pol_kv);
         }
+      };
+      // logical page lp of sequence b; a length beyond the block table is reported, and no entry
+      // past the row is read
+      auto page_of = [&](int b, int lp) {
+        if (lp >= args.max_pages) {
+          atomicCAS(&g_mla_error, 0, 1);
+          lp = args.max_pages - 1;
+        }
+        return args.block_table[(int64_t)b * args.max_pages + lp];
+      };
+      // The unit's first tile is (its first query block, its first tile): the planner makes both
+      // non-empty.  That page and the block's RoPE-query half go out straight from the unit
+      // record, before the walk over the lengths.
+      mbar_arrive_expect_tx(bar(B_QR_FULL), 8192);
+      tma_load_3d(base + SM_QR, &args.map_qr, bar(B_QR_FULL), 32 * half, 0, walker0.first_qb, pol_q);
+      load_page(0, page_of(walker0.first_qb / args.s_q, walker0.tile_begin));
+      TileCursor cur;
+      cur.init(walker0);
+      TileInfo ti;
+      PieceWalker ahead = walker0;  // one piece ahead of the tile walk
+      Piece np;
+      ahead.next(np);  // piece 0
+      int next_qb = -1, prev_qb = -1, prev_split = 0;
+      uint32_t t = 0, piece_no = 0;
+      while (cur.next(ti)) {
+        if (ti.first) {
+          if (piece_no > 0) {
+            if (!wait_one(bar(B_QR_EMPTY), (piece_no - 1) & 1, wc, kSiteQEmpty)) break;
+            mbar_arrive_expect_tx(bar(B_QR_FULL), 8192);
+            tma_load_3d(base + SM_QR, &args.map_qr, bar(B_QR_FULL), 32 * half, 0, ti.qb, pol_q);
+          }
+          ++piece_no;
+          next_qb = ahead.next(np) ? np.qb : -1;
+        }
+        const uint32_t st = t % kStages, ph = (t / kStages) & 1;
+        if (t > 0 && !wait_one(bar(B_KV_EMPTY + st), ph ^ 1, wc, kSiteKvEmpty)) break;
+        {  // the tile's schedule entry for the softmax warpgroups
+          const uint32_t e = base + SM_TI + (t % kTiRing) * 32;
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(e), "r"(ti.qb), "r"(ti.valid), "r"(ti.split),
+                       "r"((ti.first ? 1 : 0) | (ti.last ? 2 : 0))
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(e + 16), "r"((int)piece_no - 1), "r"(next_qb),
+                       "r"(prev_qb), "r"(prev_split)
+                       : "memory");
+          mbar_arrive(bar(B_TI_FULL + (t % kTiRing)));
+          prev_qb = ti.qb;
+          prev_split = ti.split;
+        }
+        if (t > 0) load_page(st, page_of(ti.qb / args.s_q, ti.tile));  // (tile 0's page went out above)
         ++t;
       }
     }
@@ -716,11 +734,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
       tc_fence_before();
     };
 
-    if (w == 0) {  // piece 0's query half
-      PieceWalker pw = walker0;
-      Piece p0;
-      if (pw.next(p0)) load_q_tmem(p0.qb);
-    }
+    if (w == 0) load_q_tmem(walker0.first_qb);  // piece 0's query half (the planner makes piece 0 non-empty)
     int np_qb = -1;  // query block of the piece after the current tile's (from the schedule)
 
     float l_mine = 0.f, m_ref = 0.f;  // this warpgroup's part of the row sum, relative to m_ref
