@@ -360,6 +360,44 @@ def time_workload(w, name, peaks, steps, warmup, dev, flush, dist=None):
     return res
 
 
+def time_projections(w, peaks, steps, warmup, dev, flush, d_nope=128, d_v=128):
+    """Median time of mla_absorb_query and mla_project_output for the workload's B*s_q tokens, with
+    their roofline (bytes: weights + activations in and out; FLOPs: 2*T*H*K*N)."""
+    import torch
+    from mla_absorbed_decode_02_gb300 import mla_absorb_query, mla_device_error, mla_project_output
+    T, H = w.batch * w.s_q, w.num_heads
+    g = torch.Generator(device=dev).manual_seed(5)
+    q_n = torch.randn((T, H, d_nope), generator=g, device=dev).to(torch.bfloat16)
+    w_uk = (torch.randn((H, d_nope, 512), generator=g, device=dev) / 512 ** 0.5).to(torch.bfloat16)
+    w_uv = (torch.randn((H, 512, d_v), generator=g, device=dev) / 512 ** 0.5).to(torch.bfloat16)
+    q_abs = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    o = torch.empty((T, H, d_v), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for name, call, K, N in (("absorb", lambda: mla_absorb_query(q_n, w_uk, q_abs, stream), d_nope, 512),
+                             ("project", lambda: mla_project_output(q_abs, w_uv, o, stream), 512, d_v)):
+        for _ in range(warmup):
+            flush.zero_()
+            call()
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b) / 1e3)
+        t = statistics.median(ts)
+        nbytes = 2 * (H * K * N + T * H * (K + N))
+        flops = 2 * T * H * K * N
+        t_roof, bound = roofline_time_s(flops, nbytes, peaks)
+        out[name] = {"us": t * 1e6, "tokens": T, "heads": H, "k": K, "n": N, "bytes": nbytes, "flops": flops,
+                     "bound": bound, "roofline_frac": t_roof / t}
+    assert mla_device_error(clear=True) == 0
+    return out
+
+
 def run_ours(args, w, peaks, world, rank, local):
     import torch
     import mla_workloads as mw
@@ -444,6 +482,10 @@ def run_ours(args, w, peaks, world, rank, local):
         "clocks": clk,
         "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops", "source")},
     }
+
+    # ---- the projections around the decode for this batch (query absorption before it, the value
+    # projection after it): random DeepSeek-V3-shaped W_UK / W_UV, L2 flushed before each call
+    res["projections"] = time_projections(w, peaks, args.steps, args.warmup, dev, flush)
 
     # ---- the other benchmark workloads (one GPU: the driver's multi-GPU runs time the headline only)
     if world == 1 and not args.no_per_config:

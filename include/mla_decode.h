@@ -186,6 +186,38 @@ int32_t mla_resolve_num_units(const mla_decode_params* p, int32_t* num_units);
 int32_t mla_quantize_kv_fp8(const void* kv_bf16, void* kv_fp8, int64_t num_tokens, void* stream);
 
 /*
+ * Query absorption ("MLA inference: two computation paths and FlashMLA", section "Two
+ * equivalent paths", path two: W_UK is folded into the query; "MLA: what the multi-head
+ * latent attention paper actually says", section "The absorbed form: how inference actually
+ * works"): for every token t and head h
+ *     q_absorbed[t][h][:] = q_nope[t][h][:] . W_UK[h]          (512 = d_c columns)
+ *   n_tokens    T >= 1 (B * s_q of a decode step)
+ *   num_heads   H, 1..65535
+ *   d_nope      per-head no-RoPE query dims (128 in DeepSeek-V3); a multiple of 64, <= 4096
+ *   q_nope      device bf16 [T][H][d_nope]
+ *   w_uk        device bf16 [H][d_nope][512]
+ *   q_absorbed  device bf16 [T][H][512]: the q_nope_absorbed input of mla_decode
+ * bf16 inputs, fp32 accumulation on the tensor cores, bf16 output (rounded to nearest even).
+ * Buffers 16-byte aligned; asynchronous on stream (a programmatic dependent of the kernel
+ * before it).  Unsupported sizes return MLA_ERR_UNSUPPORTED before any launch.
+ */
+int32_t mla_absorb_query(int32_t n_tokens, int32_t num_heads, int32_t d_nope, const void* q_nope, const void* w_uk,
+                         void* q_absorbed, void* stream);
+
+/*
+ * Value projection, the last step of the absorbed path (same sections: W_UV applied to the
+ * latent output): for every token t and head h
+ *     out[t][h][:] = o_latent[t][h][:] . W_UV[h]               (d_v columns)
+ *   o_latent    device bf16 [T][H][512]: the out of mla_decode (bf16 output)
+ *   w_uv        device bf16 [H][512][d_v]
+ *   d_v         per-head value dims (128 in DeepSeek-V3); a multiple of 64, <= 4096
+ *   out         device bf16 [T][H][d_v]
+ * Same arithmetic, alignment and error rules as mla_absorb_query.
+ */
+int32_t mla_project_output(int32_t n_tokens, int32_t num_heads, int32_t d_v, const void* o_latent, const void* w_uv,
+                           void* out, void* stream);
+
+/*
  * Device error word of the current device: synchronises the device, writes the
  * word to *word (MLA_OK if none; MLA_ERR_TIMEOUT + 16 * site for a bounded wait that ran
  * out; MLA_ERR_INVALID_ARG for a length beyond the block table; MLA_ERR_WORKSPACE for

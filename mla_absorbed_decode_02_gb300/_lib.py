@@ -72,6 +72,8 @@ def load_library():
             "mla_wait_selftest": ([i32, vp], i32),
             "mla_decode_noalloc": ([P, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp], i32),
             "mla_quantize_kv_fp8": ([vp, vp, ctypes.c_int64, vp], i32),
+            "mla_absorb_query": ([i32, i32, i32, vp, vp, vp, vp], i32),
+            "mla_project_output": ([i32, i32, i32, vp, vp, vp, vp], i32),
             "mla_status_string": ([i32], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -171,6 +173,25 @@ def mla_quantize_kv_fp8(kv_bf16, kv_fp8, num_tokens: int, stream=None):
     """bf16 cache rows [n, 576] -> 656-byte FP8 rows [n, 656] (codes, tile scales, RoPE)."""
     _check(load_library().mla_quantize_kv_fp8(_ptr(kv_bf16), _ptr(kv_fp8), int(num_tokens), _stream(stream)),
            "mla_quantize_kv_fp8")
+
+
+def mla_absorb_query(q_nope, w_uk, q_absorbed, stream=None):
+    """q_absorbed[t, h] = q_nope[t, h] @ w_uk[h]: q_nope bf16 [..., H, d_nope], w_uk bf16 [H, d_nope, 512],
+    q_absorbed bf16 [..., H, 512] (leading dims flattened to tokens)."""
+    H, d_nope = int(q_nope.shape[-2]), int(q_nope.shape[-1])
+    T = int(q_nope.numel() // (H * d_nope))
+    _check(load_library().mla_absorb_query(T, H, d_nope, _ptr(q_nope), _ptr(w_uk), _ptr(q_absorbed), _stream(stream)),
+           "mla_absorb_query")
+
+
+def mla_project_output(o_latent, w_uv, out, stream=None):
+    """out[t, h] = o_latent[t, h] @ w_uv[h]: o_latent bf16 [..., H, 512], w_uv bf16 [H, 512, d_v],
+    out bf16 [..., H, d_v] (leading dims flattened to tokens)."""
+    H = int(o_latent.shape[-2])
+    T = int(o_latent.numel() // (H * 512))
+    d_v = int(w_uv.shape[-1])
+    _check(load_library().mla_project_output(T, H, d_v, _ptr(o_latent), _ptr(w_uv), _ptr(out), _stream(stream)),
+           "mla_project_output")
 
 
 def mla_device_error(clear: bool = True) -> int:

@@ -13,6 +13,7 @@
 
 #include "../../include/mla_decode.h"
 #include "decode_kernel.cuh"
+#include "head_gemm.cuh"
 
 namespace mla {
 
@@ -592,6 +593,80 @@ int32_t mla_quantize_kv_fp8(const void* kv_bf16, void* kv_fp8, int64_t num_token
   mla_quantize_fp8_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const __nv_bfloat16*>(kv_bf16), static_cast<uint8_t*>(kv_fp8), num_tokens);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+// Per-head GEMM C[t, h, :] = A[t, h, :] . W[h] (K x N per head), bf16 in and out, fp32 accumulation.
+static int32_t launch_head_gemm(int32_t T, int32_t H, int32_t K, int32_t N, const void* a, const void* w, void* c,
+                                void* stream) {
+  if (T < 1 || H < 1 || H > 65535 || !a || !w || !c) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(w) || !aligned16(c)) return MLA_ERR_INVALID_ARG;
+  if (K < 64 || K % 64 != 0 || N < 64 || N % 64 != 0 || K > 4096 || N > 4096) return MLA_ERR_UNSUPPORTED;
+  if ((int64_t)T * H * (K > N ? K : N) > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  DeviceInfo* dinfo = nullptr;
+  int32_t st = device_info(&dinfo);
+  if (st != MLA_OK) return st;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ERR_CUDA;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(mla_head_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kHgSmemMax) !=
+        cudaSuccess)
+      return MLA_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  HeadGemmArgs g;
+  std::memset(&g, 0, sizeof g);
+  {
+    const uint64_t d[3] = {(uint64_t)K, (uint64_t)H, (uint64_t)T};
+    const uint64_t s[2] = {(uint64_t)K * 2, (uint64_t)H * K * 2};
+    const uint32_t bx[3] = {64, 1, (uint32_t)kHgRows};
+    if ((st = encode_map(&g.map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+  {
+    const uint64_t d[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)H};
+    const uint64_t s[2] = {(uint64_t)N * 2, (uint64_t)K * N * 2};
+    const uint32_t bx[3] = {64, (uint32_t)kHgKChunk, 1};
+    if ((st = encode_map(&g.map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+  g.c = c;
+  g.T = T;
+  g.H = H;
+  g.K = K;
+  g.N = N;
+  g.n_tile = N % kHgMaxN == 0 ? kHgMaxN : (N % 128 == 0 ? 128 : 64);
+  g.timeout_ns = 2000000000ull;
+  // K chunks in flight: all of them (up to six, 192 KB) when the grid fits one CTA per SM, two
+  // (two CTAs per SM) when it is larger
+  const int64_t ctas = (int64_t)(N / g.n_tile) * H * ((T + kHgRows - 1) / kHgRows);
+  const int nk = K / kHgKChunk;
+  const uint32_t sb = hg_stage_bytes(g.n_tile);
+  int stages = ctas <= dinfo->sm_count ? (int)(196608 / sb) : 2;
+  stages = stages > kHgMaxStages ? kHgMaxStages : stages;
+  stages = stages > nk ? nk : stages;
+  g.stages = stages < 2 ? 2 : stages;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(N / g.n_tile, H, (T + kHgRows - 1) / kHgRows);
+  cfg.blockDim = dim3(kHgThreads, 1, 1);
+  cfg.dynamicSmemBytes = g.stages * sb + 1024 + kHgTail;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_head_gemm_kernel, g) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int32_t mla_absorb_query(int32_t n_tokens, int32_t num_heads, int32_t d_nope, const void* q_nope, const void* w_uk,
+                         void* q_absorbed, void* stream) {
+  return launch_head_gemm(n_tokens, num_heads, d_nope, 512, q_nope, w_uk, q_absorbed, stream);
+}
+
+int32_t mla_project_output(int32_t n_tokens, int32_t num_heads, int32_t d_v, const void* o_latent, const void* w_uv,
+                           void* out, void* stream) {
+  return launch_head_gemm(n_tokens, num_heads, 512, d_v, o_latent, w_uv, out, stream);
 }
 
 int32_t mla_wait_selftest(int32_t timeout_us, void* stream) {

@@ -188,3 +188,20 @@ def from_workload(w) -> Problem:
     return Problem(q_nope=bf16_bits_to_f64(w.q_nope), q_rope=bf16_bits_to_f64(w.q_rope), kv=w.kv, kv_kind=kind,
                    block_table=w.block_table, seqlens=w.seqlens, scale=w.scale, causal=w.causal,
                    page_size=w.page_size)
+
+
+def absorb_query(q_nope, w_uk) -> np.ndarray:
+    """q~[.., h, :] = q^N[.., h, :] W_UK[h]: the query absorption of the absorbed path ("MLA
+    inference: two computation paths and FlashMLA", section "Two equivalent paths", path two),
+    in float64.  q_nope [..., H, d_nope], w_uk [H, d_nope, d_c] -> [..., H, d_c]."""
+    q = np.asarray(q_nope, np.float64)
+    w = np.asarray(w_uk, np.float64)
+    return np.einsum("...hk,hkn->...hn", q, w)
+
+
+def project_output(o_latent, w_uv) -> np.ndarray:
+    """o[.., h, :] = o~[.., h, :] W_UV[h]: the value projection that ends the absorbed path (same
+    section), in float64.  o_latent [..., H, d_c], w_uv [H, d_c, d_v] -> [..., H, d_v]."""
+    o = np.asarray(o_latent, np.float64)
+    w = np.asarray(w_uv, np.float64)
+    return np.einsum("...hk,hkn->...hn", o, w)

@@ -216,3 +216,15 @@ def test_plan_refuses_more_positions_than_an_int32_holds(lib):
     ok = np.full(B, 1 << 19, np.int32)                   # 8192 tiles + 6 each: below 2^31
     sched = _lib.mla_plan_host(p, 76, ok)
     assert sched[0] == _lib.SCHED_MAGIC and sched[1] == 76 and sched[2] == B
+
+
+def test_head_projections_reject_bad_arguments_before_any_launch(lib):
+    """mla_absorb_query / mla_project_output check their sizes and pointers before touching CUDA."""
+    buf = ctypes.c_void_p(256)  # never dereferenced
+    odd = ctypes.c_void_p(258)  # not 16-byte aligned
+    for f in (lib.mla_absorb_query, lib.mla_project_output):
+        assert f(0, 128, 128, buf, buf, buf, None) == _lib.MLA_ERR_INVALID_ARG         # no tokens
+        assert f(4, 0, 128, buf, buf, buf, None) == _lib.MLA_ERR_INVALID_ARG           # no heads
+        assert f(4, 128, 128, None, buf, buf, None) == _lib.MLA_ERR_INVALID_ARG        # null input
+        assert f(4, 128, 128, buf, buf, odd, None) == _lib.MLA_ERR_INVALID_ARG         # misaligned output
+        assert f(4, 128, 100, buf, buf, buf, None) == _lib.MLA_ERR_UNSUPPORTED         # width not a multiple of 64

@@ -109,12 +109,12 @@ def test_absorb_equals_expand(H, NOPE, ROPE, DV, DC, L, s_q, page):
         out1[:, hh] = p @ v
 
     # path two: absorb W_uk into the query, attend over the paged latent cache, apply W_uv last
-    q_lat = np.einsum("thn,hcn->thc", q_n[new], W_uk)       # [s_q, H, DC]
+    q_lat = oracle.absorb_query(q_n[new], W_uk.transpose(0, 2, 1))   # [s_q, H, DC]; W_uk[h]^T is [NOPE, DC]
     pool, bt = paged([np.concatenate([c, k_r], axis=1)], page, rng)
     P = Problem(q_nope=q_lat[None], q_rope=q_r[new][None], kv=pool, kv_kind=KV_F64, block_table=bt,
                 seqlens=np.array([L], np.int32), scale=scale, causal=True, page_size=page)
     out_lat, _ = P.full()
-    out2 = np.einsum("thc,hcv->thv", out_lat[0], W_uv)
+    out2 = oracle.project_output(out_lat[0], W_uv)
     np.testing.assert_allclose(out2, out1, rtol=1e-10, atol=1e-12)
 
 
@@ -390,3 +390,23 @@ def test_from_workload_matches_a_problem_built_by_hand(kv_dtype):
     c = Problem(widen(w.q_nope), widen(w.q_rope), pool, KV_F64, w.block_table, w.seqlens, 1 / math.sqrt(192),
                 causal=True, page_size=64).full()
     assert not np.array_equal(a[1][:, 0], c[1][:, 0])
+
+
+def test_head_projections_by_loops():
+    """oracle.absorb_query / project_output against sums written out element by element."""
+    rng = np.random.default_rng(77)
+    T, H, K, N = 3, 2, 5, 4
+    a = rng.standard_normal((T, H, K))
+    w = rng.standard_normal((H, K, N))
+    want = np.zeros((T, H, N))
+    for t in range(T):
+        for h in range(H):
+            for n in range(N):
+                acc = 0.0
+                for k in range(K):
+                    acc += a[t, h, k] * w[h, k, n]
+                want[t, h, n] = acc
+    np.testing.assert_allclose(oracle.absorb_query(a, w), want, rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(oracle.project_output(a, w), want, rtol=1e-14, atol=1e-14)
+    # head h uses only W[h]: swapping the heads' weights swaps the heads' outputs
+    np.testing.assert_allclose(oracle.absorb_query(a, w[::-1])[:, 0], oracle.absorb_query(a[:, ::-1], w)[:, 1])
