@@ -205,3 +205,65 @@ def project_output(o_latent, w_uv) -> np.ndarray:
     o = np.asarray(o_latent, np.float64)
     w = np.asarray(w_uv, np.float64)
     return np.einsum("...hk,hkn->...hn", o, w)
+
+
+# ---------------------------------------------------------------- the expand path (extend)
+
+def round_bf16(x) -> np.ndarray:
+    """Round float64 values to the nearest bf16 value, ties to even, returned as float64 (for
+    values in bf16's normal range; zero stays zero).  bf16 keeps 8 significant bits: write
+    x = m * 2^e with m in [0.5, 1), round m * 2^8 to an integer (numpy rounds halves to even)."""
+    m, e = np.frexp(np.asarray(x, np.float64))
+    return np.ldexp(np.round(m * 256.0), e - 8)
+
+
+def cache_rows(kv_bits, block_table, b: int, L: int, page_size: int = 64) -> np.ndarray:
+    """Rows 0..L-1 of sequence b's paged bf16 cache, widened to float64: [L, d_c + d_r].
+    Row j lives in slot j % page_size of page block_table[b][j // page_size]."""
+    n_pages = (L + page_size - 1) // page_size
+    pages = np.asarray(block_table[b, :n_pages], np.int64)
+    return bf16_bits_to_f64(np.asarray(kv_bits)[pages].reshape(-1, kv_bits.shape[-1])[:L])
+
+
+def expand_kv(c, w_uk, w_uv):
+    """Path one's expansion of cached latent vectors ("MLA inference: two computation paths and
+    FlashMLA", section "Two equivalent paths", path one): per head h, the non-positional key
+    k^N_j = W_UK[h] c_j and the value v_j = c_j W_UV[h], with W_UK [H, d_nope, d_c] and
+    W_UV [H, d_c, d_v] (the layouts of absorb_query / project_output).
+    c [L, d_c] -> (k^N [H, L, d_nope], v [H, L, d_v]), float64."""
+    c = np.asarray(c, np.float64)
+    return (np.einsum("hnc,jc->hjn", np.asarray(w_uk, np.float64), c),
+            np.einsum("jc,hcv->hjv", c, np.asarray(w_uv, np.float64)))
+
+
+def extend_expanded(q_nope, q_rope, kv_bits, block_table, seqlens, w_uk, w_uv, scale, page_size=64,
+                    d_c=512, round_kv=False):
+    """Extend (prefill continuation) by path one ("Two equivalent paths"; section "Which is
+    faster: count new tokens and cached tokens"): the s_q new tokens of sequence b are the last
+    s_q of its L_b cached rows; query t attends, per head, to keys j <= L_b - s_q + t with key
+    [k^N_j, k^R_j] (k^R_j stored in the cache row after the latent) and value v_j, score
+    scale * (q^N . k^N_j + q^R . k^R_j).  Plain two-pass softmax in float64.
+    round_kv: hold k^N and v as bf16 (the model's activation type) before attending.
+    q_nope [B, s_q, H, d_nope], q_rope [B, s_q, H, d_r] float64; kv_bits uint16 bf16 pages
+    -> out [B, s_q, H, d_v], lse [B, s_q, H] (natural log of the sum of exp(score))."""
+    q_nope = np.asarray(q_nope, np.float64)
+    q_rope = np.asarray(q_rope, np.float64)
+    B, s_q, H, _ = q_nope.shape
+    d_v = np.asarray(w_uv).shape[-1]
+    out = np.zeros((B, s_q, H, d_v))
+    lse = np.full((B, s_q, H), -np.inf)
+    for b in range(B):
+        L = int(seqlens[b])
+        rows = cache_rows(kv_bits, block_table, b, L, page_size)
+        kn, v = expand_kv(rows[:, :d_c], w_uk, w_uv)
+        if round_kv:
+            kn, v = round_bf16(kn), round_bf16(v)
+        s = scale * (np.einsum("thn,hjn->thj", q_nope[b], kn) + np.einsum("thr,jr->thj", q_rope[b], rows[:, d_c:]))
+        hidden = np.arange(L)[None, :] > (L - s_q + np.arange(s_q))[:, None]      # [s_q, L]
+        s[np.broadcast_to(hidden[:, None, :], s.shape)] = -np.inf
+        m = s.max(axis=-1, keepdims=True)
+        e = np.exp(s - m)
+        l = e.sum(axis=-1)
+        out[b] = np.einsum("thj,hjv->thv", e / l[..., None], v)
+        lse[b] = m[..., 0] + np.log(l)
+    return out, lse

@@ -410,3 +410,90 @@ def test_head_projections_by_loops():
     np.testing.assert_allclose(oracle.project_output(a, w), want, rtol=1e-14, atol=1e-14)
     # head h uses only W[h]: swapping the heads' weights swaps the heads' outputs
     np.testing.assert_allclose(oracle.absorb_query(a, w[::-1])[:, 0], oracle.absorb_query(a[:, ::-1], w)[:, 1])
+
+
+# ---------------------------------------------------------------- the expand path (extend)
+
+def test_round_bf16_matches_torch_cast():
+    """oracle.round_bf16 against torch's float32 -> bf16 cast (round to nearest, ties to even) on
+    float32 inputs, where a single rounding is exact: random values, exact ties and one-ulp
+    neighbours of ties."""
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(20000) * 2.0 ** rng.integers(-20, 20, 20000)).astype(np.float32)
+    bits = x.view(np.uint32)
+    ties = ((bits & np.uint32(0xFFFF0000)) | np.uint32(0x8000)).view(np.float32)
+    near = np.concatenate([(ties.view(np.uint32) + np.uint32(1)).view(np.float32),
+                           (ties.view(np.uint32) - np.uint32(1)).view(np.float32)])
+    for v in (x, ties, near, np.float32([0.0, -0.0, 1.0, -3.5])):
+        want = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+        np.testing.assert_array_equal(oracle.round_bf16(v.astype(np.float64)), want)
+
+
+def test_expand_kv_by_loops():
+    """oracle.expand_kv against sums written out element by element: k^N_j[n] = sum_c W_UK[h][n][c] c_j[c],
+    v_j[n] = sum_c c_j[c] W_UV[h][c][n]."""
+    rng = np.random.default_rng(8)
+    H, L, DC, NOPE, DV = 2, 3, 5, 4, 3
+    c = rng.standard_normal((L, DC))
+    w_uk = rng.standard_normal((H, NOPE, DC))
+    w_uv = rng.standard_normal((H, DC, DV))
+    kn, v = oracle.expand_kv(c, w_uk, w_uv)
+    for h in range(H):
+        for j in range(L):
+            for n in range(NOPE):
+                assert abs(kn[h, j, n] - sum(w_uk[h, n, k] * c[j, k] for k in range(DC))) < 1e-13
+            for n in range(DV):
+                assert abs(v[h, j, n] - sum(c[j, k] * w_uv[h, k, n] for k in range(DC))) < 1e-13
+
+
+def _bf16_pool(rows_per_seq, rng, extra_pages=2):
+    """bf16 bit patterns of per-sequence rows [L_b, 576] scattered over a shuffled page pool."""
+    pool, bt = paged(rows_per_seq, 64, rng, extra_pages)
+    bits = torch.from_numpy(pool.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return bits, bt
+
+
+@pytest.mark.parametrize("lengths,s_q", [([70, 150], 1), ([70, 150], 3), ([9, 200], 8), ([40, 40], 40)])
+def test_extend_expanded_equals_absorbed_oracle(lengths, s_q):
+    """Path one (oracle.extend_expanded, numpy) against path two computed by the C oracle on the
+    absorbed queries, then projected by W_UV ("Two equivalent paths": the two paths give the same
+    output; the lse is the same quantity on both).  Includes a pure prefill (s_q = L)."""
+    rng = np.random.default_rng(sum(lengths) + s_q)
+    B, H, NOPE, DC, DR, DV = len(lengths), 4, 128, 512, 64, 128
+    rows = [rng.standard_normal((L, DC + DR)) for L in lengths]
+    kv, bt = _bf16_pool(rows, rng)
+    q_n = rng.standard_normal((B, s_q, H, NOPE))
+    q_r = rng.standard_normal((B, s_q, H, DR))
+    w_uk = rng.standard_normal((H, NOPE, DC)) / math.sqrt(DC)
+    w_uv = rng.standard_normal((H, DC, DV)) / math.sqrt(DC)
+    seqlens = np.array(lengths, np.int32)
+    scale = 1 / math.sqrt(NOPE + DR)
+    out1, lse1 = oracle.extend_expanded(q_n, q_r, kv, bt, seqlens, w_uk, w_uv, scale)
+    P = Problem(q_nope=oracle.absorb_query(q_n, w_uk), q_rope=q_r, kv=kv, kv_kind=KV_BF16, block_table=bt,
+                seqlens=seqlens, scale=scale, causal=True)
+    out_lat, lse2 = P.full()
+    np.testing.assert_allclose(out1, oracle.project_output(out_lat, w_uv), rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(lse1, lse2, rtol=0, atol=1e-10)
+
+
+def test_extend_expanded_closed_forms():
+    """One cached row and one query: out = v_0 and lse = the score.  Two equal rows: the same
+    output and lse + ln 2."""
+    rng = np.random.default_rng(21)
+    H, NOPE, DC, DR, DV = 3, 128, 512, 64, 128
+    row = rng.standard_normal((1, DC + DR))
+    w_uk = rng.standard_normal((H, NOPE, DC)) / 16
+    w_uv = rng.standard_normal((H, DC, DV)) / 16
+    q_n = rng.standard_normal((1, 1, H, NOPE))
+    q_r = rng.standard_normal((1, 1, H, DR))
+    kv, bt = _bf16_pool([row], rng)
+    c = oracle.bf16_bits_to_f64(kv[bt[0, 0], 0])
+    kn, v = oracle.expand_kv(c[None, :DC], w_uk, w_uv)
+    out, lse = oracle.extend_expanded(q_n, q_r, kv, bt, np.array([1], np.int32), w_uk, w_uv, 0.1)
+    np.testing.assert_allclose(out[0, 0], v[:, 0], rtol=1e-12)
+    want_s = 0.1 * (np.einsum("hn,hn->h", q_n[0, 0], kn[:, 0]) + q_r[0, 0] @ c[DC:])
+    np.testing.assert_allclose(lse[0, 0], want_s, rtol=1e-12)
+    kv2, bt2 = _bf16_pool([np.concatenate([row, row])], rng)
+    out2, lse2 = oracle.extend_expanded(q_n, q_r, kv2, bt2, np.array([2], np.int32), w_uk, w_uv, 0.1)
+    np.testing.assert_allclose(out2, out, rtol=1e-12)
+    np.testing.assert_allclose(lse2, lse + math.log(2), rtol=1e-12)
