@@ -398,6 +398,58 @@ def time_projections(w, peaks, steps, warmup, dev, flush, d_nope=128, d_v=128):
     return out
 
 
+def extend_flops(q: int, k: int, H: int, d_c: int = D_C, d_nope: int = 128, d_r: int = D_R, d_v: int = 128) -> int:
+    """FLOPs of an extend by path one ("Which is faster: count new tokens and cached tokens"):
+    expanding every cached row into H keys and values, 2*d_c*H*(d_nope + d_v) each, plus the
+    causal (query, key) pairs at 2*H*(d_nope + d_r) + 2*H*d_v each."""
+    return k * 2 * d_c * H * (d_nope + d_v) + causal_pairs(q, k) * (2 * H * (d_nope + d_r) + 2 * H * d_v)
+
+
+def time_extend(peaks, steps, warmup, dev, flush, prefix=32768, s_q=512, H=128, chunk=4096):
+    """Median time of mla_extend appending s_q tokens to a `prefix`-row cache (one sequence, the
+    pages' "append 512 tokens after a 32K cached prefix"), with its tensor roofline."""
+    import torch
+    import mla_workloads as mw
+    from mla_absorbed_decode_02_gb300 import MlaExtendParams, mla_device_error, mla_extend, mla_extend_workspace_size
+    L = prefix + s_q
+    x = mw.make_extend([L], s_q=s_q, num_heads=H, seed=11, nan_tail=False)
+    c = x.cache
+    dv = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+    q_n, q_r, kv, w_uk, w_uv = dv(x.q_nope), dv(x.q_rope), dv(c.kv), dv(x.w_uk), dv(x.w_uv)
+    bt, seq = torch.from_numpy(c.block_table).to(dev), torch.from_numpy(c.seqlens).to(dev)
+    p = MlaExtendParams.make(1, s_q, H, c.kv.shape[0], c.block_table.shape[1], L, chunk)
+    ws = torch.empty(mla_extend_workspace_size(p), dtype=torch.uint8, device=dev)
+    out = torch.empty((1, s_q, H, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((1, s_q, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        mla_extend(p, q_n, q_r, kv, bt, seq, w_uk, w_uv, x.scale, out, lse, ws, stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ts.append(a.elapsed_time(b) / 1e3)
+    assert mla_device_error(clear=True) == 0
+    t = statistics.median(ts)
+    flops = extend_flops(s_q, L, H)
+    nbytes = L * 1152 + s_q * H * (128 + D_R) * 2 + 2 * H * 128 * D_C * 2 + s_q * H * (128 * 2 + 4)
+    t_roof, bound = roofline_time_s(flops, nbytes, peaks)
+    n_chunks = (L + chunk - 1) // chunk
+    return {"workload": f"append {s_q} tokens after a {prefix}-row cache (B=1, H={H}, d_nope=d_v=128)",
+            "chunk_tokens": chunk, "launches": 2 * n_chunks, "us": t * 1e6, "flops": flops, "bytes": nbytes,
+            "tflops": flops / t / 1e12, "bound": bound, "roofline_frac": t_roof / t,
+            "timing": f"median of {steps} calls after {warmup}, L2 flushed before each, CUDA events"}
+
+
 def run_ours(args, w, peaks, world, rank, local):
     import torch
     import mla_workloads as mw
@@ -487,6 +539,10 @@ def run_ours(args, w, peaks, world, rank, local):
     # projection after it): random DeepSeek-V3-shaped W_UK / W_UV, L2 flushed before each call
     res["projections"] = time_projections(w, peaks, args.steps, args.warmup, dev, flush)
 
+    # ---- the expand path for an extend (chunked prefix expansion with the LSE merge)
+    if world == 1 and not args.no_extend:
+        res["extend"] = time_extend(peaks, min(args.steps, 20), min(args.warmup, 5), dev, flush)
+
     # ---- the other benchmark workloads (one GPU: the driver's multi-GPU runs time the headline only)
     if world == 1 and not args.no_per_config:
         per = {}
@@ -522,6 +578,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="time the chosen workload only")
+    ap.add_argument("--no-extend", action="store_true", help="skip the extend (expand path) timing")
     ap.add_argument("--batch", type=int, default=0,
                     help="keep only the first B sequences of the workload (same recipe; for profiling small cases)")
     args = ap.parse_args()

@@ -218,6 +218,77 @@ int32_t mla_project_output(int32_t n_tokens, int32_t num_heads, int32_t d_v, con
                            void* out, void* stream);
 
 /*
+ * Extend by the expand path, chunk by chunk ("MLA inference: two computation paths and
+ * FlashMLA", section "Two equivalent paths", path one, and section "Which is faster: count
+ * new tokens and cached tokens": with many new tokens the keys and values are expanded per
+ * head and attended as ordinary multi-head attention; a long prefix is expanded a chunk at a
+ * time and the chunks' results are merged by their log-sum-exp).  Sequence b has L_b cached
+ * rows, the last s_q of them its new tokens; new token t attends to rows 0 .. L_b - s_q + t.
+ */
+typedef struct mla_extend_params {
+  int32_t batch;             /* B >= 1 sequences (<= 65535) */
+  int32_t s_q;               /* new tokens per sequence, >= 1, already written into the cache */
+  int32_t num_heads;         /* H, 1..128 */
+  int32_t d_nope;            /* per-head no-RoPE query/key dims; must be 128 */
+  int32_t d_v;               /* per-head value dims; must be 128 */
+  int32_t num_pages;         /* physical pages in the pool (>= 1) */
+  int32_t page_size;         /* must be 64 */
+  int32_t max_pages_per_seq; /* row length of block_table (>= 1) */
+  int32_t max_seqlen;        /* an upper bound of every L_b, s_q <= max_seqlen <= 64 * max_pages_per_seq;
+                                it fixes the number of chunks, ceil(max_seqlen / chunk_tokens) */
+  int32_t chunk_tokens;      /* C: cached rows expanded at a time; a multiple of 128 */
+  int32_t timeout_us;        /* limit of every bounded wait inside the kernels; 0 = 2,000,000 us */
+  int32_t reserved[5];       /* must be zero */
+} mla_extend_params;
+
+/*
+ * Size of the device workspace mla_extend needs for p: the expanded keys and values of one
+ * chunk (bf16, 2 * B * H * C * 128 * 2 bytes) and the float32 accumulators of the merge
+ * (B * s_q * H * 129 * 4 bytes), each rounded up to 256 bytes.  Host only.
+ */
+int32_t mla_extend_workspace_size(const mla_extend_params* p, size_t* workspace_bytes);
+
+/*
+ * The expansion of one chunk (path one's per-head keys and values): for every sequence b,
+ * head h and row j of [chunk_start, chunk_start + C)
+ *     k_nope[b][h][j - chunk_start][:] = W_UK[h] . c_j      (d_nope values)
+ *     v[b][h][j - chunk_start][:]      = c_j . W_UV[h]      (d_v values)
+ * with c_j the 512 latent values of cache row j; rows j >= L_b are written as zeros, except
+ * whole 128-row tiles at or past L_b, which are not written.
+ *   kv_pages      device bf16 [num_pages][64][576] (the MLA_KV_BF16 layout)
+ *   block_table   device int32 [B][max_pages_per_seq]; cache_seqlens device int32 [B]
+ *                 (a length < s_q or > 64 * max_pages_per_seq sets MLA_ERR_INVALID_ARG in the
+ *                 device error word and that sequence is skipped)
+ *   w_uk          device bf16 [H][d_nope][512]; w_uv device bf16 [H][512][d_v] (the layouts
+ *                 of mla_absorb_query and mla_project_output)
+ *   chunk_start   a multiple of chunk_tokens, >= 0
+ *   k_nope, v     device bf16 [B][H][chunk_tokens][128]
+ * bf16 inputs, fp32 accumulation on the tensor cores, bf16 outputs rounded to nearest even.
+ * Buffers 16-byte aligned; asynchronous on stream.
+ */
+int32_t mla_expand_kv(const mla_extend_params* p, const void* kv_pages, const int32_t* block_table,
+                      const int32_t* cache_seqlens, const void* w_uk, const void* w_uv, int32_t chunk_start,
+                      void* k_nope, void* v, void* stream);
+
+/*
+ * The extend: for each chunk of C rows, mla_expand_kv into the workspace, then attention of
+ * every new token over the chunk's rows it may see,
+ *     score_j = scale * (q_nope . k^N_j + q_rope . k^R_j)     (k^R_j: the 64 RoPE values of row j)
+ * with an online softmax, merged with the chunks before by their log-sum-exp (float32).
+ *   q_nope   device bf16 [B][s_q][H][128]; q_rope device bf16 [B][s_q][H][64]
+ *   kv_pages, block_table, cache_seqlens, w_uk, w_uv   as for mla_expand_kv
+ *   scale    softmax scale, finite and > 0 (1/sqrt(192) for DeepSeek-V3 shapes)
+ *   out      device bf16 [B][s_q][H][d_v]: softmax-weighted sum of the values
+ *   lse      device float32 [B][s_q][H]: natural log of the sum of exp(score) over the visible rows
+ *   workspace  device, mla_extend_workspace_size(p) bytes, 256-byte aligned
+ * Keys and values are held in bf16 between the two kernels, P in bf16 for the P.V product.
+ * 2 * ceil(max_seqlen / C) launches on stream, each a programmatic dependent of the one before.
+ */
+int32_t mla_extend(const mla_extend_params* p, const void* q_nope, const void* q_rope, const void* kv_pages,
+                   const int32_t* block_table, const int32_t* cache_seqlens, const void* w_uk, const void* w_uv,
+                   float scale, void* out, float* lse, void* workspace, void* stream);
+
+/*
  * Device error word of the current device: synchronises the device, writes the
  * word to *word (MLA_OK if none; MLA_ERR_TIMEOUT + 16 * site for a bounded wait that ran
  * out; MLA_ERR_INVALID_ARG for a length beyond the block table; MLA_ERR_WORKSPACE for

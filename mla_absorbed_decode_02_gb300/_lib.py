@@ -48,6 +48,19 @@ class MlaDecodeParams(ctypes.Structure):
                    out_dtype, num_units, timeout_us)
 
 
+class MlaExtendParams(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("s_q", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("d_nope", ctypes.c_int32), ("d_v", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32), ("max_seqlen", ctypes.c_int32),
+                ("chunk_tokens", ctypes.c_int32), ("timeout_us", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
+
+    @classmethod
+    def make(cls, batch, s_q, num_heads, num_pages, max_pages_per_seq, max_seqlen, chunk_tokens=4096, d_nope=128,
+             d_v=128, timeout_us=0, page_size=64):
+        return cls(batch, s_q, num_heads, d_nope, d_v, num_pages, page_size, max_pages_per_seq, max_seqlen,
+                   chunk_tokens, timeout_us)
+
+
 def load_library():
     """Load the built library (raises if it has not been built)."""
     global _lib
@@ -59,6 +72,7 @@ def load_library():
             raise ImportError(f"{path} is missing: build it with mla_absorbed_decode_02_gb300.build.build()")
         lib = ctypes.CDLL(path)
         P = ctypes.POINTER(MlaDecodeParams)
+        X = ctypes.POINTER(MlaExtendParams)
         vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
         sig = {
             "mla_get_workspace_size": ([P, ctypes.POINTER(sz), ctypes.POINTER(sz)], i32),
@@ -74,6 +88,9 @@ def load_library():
             "mla_quantize_kv_fp8": ([vp, vp, ctypes.c_int64, vp], i32),
             "mla_absorb_query": ([i32, i32, i32, vp, vp, vp, vp], i32),
             "mla_project_output": ([i32, i32, i32, vp, vp, vp, vp], i32),
+            "mla_extend_workspace_size": ([X, ctypes.POINTER(sz)], i32),
+            "mla_expand_kv": ([X, vp, vp, vp, vp, vp, i32, vp, vp, vp], i32),
+            "mla_extend": ([X, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp], i32),
             "mla_status_string": ([i32], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -192,6 +209,29 @@ def mla_project_output(o_latent, w_uv, out, stream=None):
     d_v = int(w_uv.shape[-1])
     _check(load_library().mla_project_output(T, H, d_v, _ptr(o_latent), _ptr(w_uv), _ptr(out), _stream(stream)),
            "mla_project_output")
+
+
+def mla_extend_workspace_size(p: MlaExtendParams) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().mla_extend_workspace_size(ctypes.byref(p), ctypes.byref(n)), "mla_extend_workspace_size")
+    return n.value
+
+
+def mla_expand_kv(p: MlaExtendParams, kv_pages, block_table, cache_seqlens, w_uk, w_uv, chunk_start: int, k_nope, v,
+                  stream=None):
+    """k_nope[b, h, j] = w_uk[h] @ c_j and v[b, h, j] = c_j @ w_uv[h] for cache rows j of one chunk:
+    k_nope, v bf16 [B, H, chunk_tokens, 128]."""
+    _check(load_library().mla_expand_kv(ctypes.byref(p), _ptr(kv_pages), _ptr(block_table), _ptr(cache_seqlens),
+                                        _ptr(w_uk), _ptr(w_uv), int(chunk_start), _ptr(k_nope), _ptr(v),
+                                        _stream(stream)), "mla_expand_kv")
+
+
+def mla_extend(p: MlaExtendParams, q_nope, q_rope, kv_pages, block_table, cache_seqlens, w_uk, w_uv, scale: float,
+               out, lse, workspace, stream=None):
+    """Extend by the expand path, chunk by chunk: out bf16 [B, s_q, H, 128], lse float32 [B, s_q, H]."""
+    _check(load_library().mla_extend(ctypes.byref(p), _ptr(q_nope), _ptr(q_rope), _ptr(kv_pages), _ptr(block_table),
+                                     _ptr(cache_seqlens), _ptr(w_uk), _ptr(w_uv), float(scale), _ptr(out), _ptr(lse),
+                                     _ptr(workspace), _stream(stream)), "mla_extend")
 
 
 def mla_device_error(clear: bool = True) -> int:

@@ -14,6 +14,7 @@
 #include "../../include/mla_decode.h"
 #include "decode_kernel.cuh"
 #include "head_gemm.cuh"
+#include "extend_kernel.cuh"
 
 namespace mla {
 
@@ -667,6 +668,212 @@ int32_t mla_absorb_query(int32_t n_tokens, int32_t num_heads, int32_t d_nope, co
 int32_t mla_project_output(int32_t n_tokens, int32_t num_heads, int32_t d_v, const void* o_latent, const void* w_uv,
                            void* out, void* stream) {
   return launch_head_gemm(n_tokens, num_heads, 512, d_v, o_latent, w_uv, out, stream);
+}
+
+// ------------------------------------------------------------------ extend by the expand path
+static int32_t check_extend(const mla_extend_params* p) {
+  if (!p) return MLA_ERR_INVALID_ARG;
+  if (p->batch < 1 || p->s_q < 1 || p->num_heads < 1 || p->num_pages < 1 || p->max_pages_per_seq < 1 ||
+      p->max_seqlen < 1 || p->chunk_tokens < 1 || p->timeout_us < 0)
+    return MLA_ERR_INVALID_ARG;
+  for (int i = 0; i < 5; ++i)
+    if (p->reserved[i] != 0) return MLA_ERR_INVALID_ARG;
+  if (p->s_q > p->max_seqlen || (int64_t)p->max_seqlen > (int64_t)p->max_pages_per_seq * 64) return MLA_ERR_INVALID_ARG;
+  if (p->page_size != 64 || p->d_nope != kXDim || p->d_v != kXDim || p->num_heads > 128 || p->chunk_tokens % 128 != 0)
+    return MLA_ERR_UNSUPPORTED;
+  if (p->batch > 65535 || (int64_t)p->num_pages * 64 > INT32_MAX || (int64_t)p->batch * p->num_heads > INT32_MAX ||
+      (int64_t)p->batch * p->s_q * p->num_heads > INT32_MAX)
+    return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+struct ExtendLayout {
+  size_t kv, acc_o, acc_lse, total;  // bytes of K^N (and of V), of the output and lse accumulators
+};
+static ExtendLayout extend_layout(const mla_extend_params* p) {
+  ExtendLayout l;
+  l.kv = align256((size_t)p->batch * p->num_heads * p->chunk_tokens * kXDim * 2);
+  l.acc_o = align256((size_t)p->batch * p->s_q * p->num_heads * kXDim * 4);
+  l.acc_lse = align256((size_t)p->batch * p->s_q * p->num_heads * 4);
+  l.total = 2 * l.kv + l.acc_o + l.acc_lse;
+  return l;
+}
+
+static void pdl_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, void* stream) {
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+  cfg->stream = static_cast<cudaStream_t>(stream);
+}
+
+static int32_t extend_attrs(DeviceInfo** dinfo) {
+  int32_t st = device_info(dinfo);
+  if (st != MLA_OK) return st;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ERR_CUDA;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(mla_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kExSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAtSmem) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  return MLA_OK;
+}
+
+static int32_t cache_map(CUtensorMap* m, const void* kv_pages, int32_t num_pages) {
+  const uint64_t d[2] = {576, (uint64_t)num_pages * 64};
+  const uint64_t s[1] = {576 * 2};
+  const uint32_t bx[2] = {64, 64};
+  return encode_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_pages, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+static int32_t workspace_map(CUtensorMap* m, const void* buf, const mla_extend_params* p) {
+  const uint64_t d[3] = {(uint64_t)kXDim, (uint64_t)p->chunk_tokens, (uint64_t)p->batch * p->num_heads};
+  const uint64_t s[2] = {(uint64_t)kXDim * 2, (uint64_t)p->chunk_tokens * kXDim * 2};
+  const uint32_t bx[3] = {64, 64, 1};
+  return encode_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, buf, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Maps and grid of the expansion; the caller sets chunk_start and launches.
+static int32_t expand_setup(const mla_extend_params* p, const void* kv_pages, const int32_t* block_table,
+                            const int32_t* cache_seqlens, const void* w_uk, const void* w_uv, void* k_nope, void* v,
+                            int sm_count, ExpandArgs* a, dim3* grid) {
+  std::memset(a, 0, sizeof *a);
+  int32_t st;
+  if ((st = cache_map(&a->map_kvc, kv_pages, p->num_pages))) return st;
+  {
+    const uint64_t d[3] = {512, (uint64_t)kXDim, (uint64_t)p->num_heads};
+    const uint64_t s[2] = {512 * 2, (uint64_t)kXDim * 512 * 2};
+    const uint32_t bx[3] = {64, 128, 1};
+    if ((st = encode_map(&a->map_wuk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w_uk, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+  {
+    const uint64_t d[3] = {(uint64_t)kXDim, 512, (uint64_t)p->num_heads};
+    const uint64_t s[2] = {(uint64_t)kXDim * 2, (uint64_t)512 * kXDim * 2};
+    const uint32_t bx[3] = {64, 64, 1};
+    if ((st = encode_map(&a->map_wuv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w_uv, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+  }
+  a->block_table = block_table;
+  a->seqlens = cache_seqlens;
+  a->kn = static_cast<__nv_bfloat16*>(k_nope);
+  a->v = static_cast<__nv_bfloat16*>(v);
+  a->B = p->batch;
+  a->H = p->num_heads;
+  a->C = p->chunk_tokens;
+  a->s_q = p->s_q;
+  a->max_pages_per_seq = p->max_pages_per_seq;
+  a->timeout_ns = (uint64_t)(p->timeout_us ? p->timeout_us : 2000000) * 1000ull;
+  // heads per CTA: as many as keep at least two CTAs per SM busy (the latent tile is loaded once
+  // per CTA and reused for all of its heads)
+  const int64_t tiles = (int64_t)(p->chunk_tokens / 128) * p->batch;
+  int hpc = 1;
+  for (int c : {8, 4, 2})
+    if (p->num_heads % c == 0 && tiles * (p->num_heads / c) >= 2 * sm_count) {
+      hpc = c;
+      break;
+    }
+  a->heads_per_cta = hpc;
+  *grid = dim3(p->chunk_tokens / 128, p->batch, p->num_heads / hpc);
+  return MLA_OK;
+}
+
+static int32_t launch_expand(const ExpandArgs& a, dim3 grid, void* stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kXThreads, 1, 1);
+  cfg.dynamicSmemBytes = kExSmem;
+  pdl_config(&cfg, attr, stream);
+  return cudaLaunchKernelEx(&cfg, mla_expand_kernel, a) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int32_t mla_extend_workspace_size(const mla_extend_params* p, size_t* workspace_bytes) {
+  int32_t st = check_extend(p);
+  if (st != MLA_OK) return st;
+  if (!workspace_bytes) return MLA_ERR_INVALID_ARG;
+  *workspace_bytes = extend_layout(p).total;
+  return MLA_OK;
+}
+
+int32_t mla_expand_kv(const mla_extend_params* p, const void* kv_pages, const int32_t* block_table,
+                      const int32_t* cache_seqlens, const void* w_uk, const void* w_uv, int32_t chunk_start,
+                      void* k_nope, void* v, void* stream) {
+  int32_t st = check_extend(p);
+  if (st != MLA_OK) return st;
+  if (!kv_pages || !block_table || !cache_seqlens || !w_uk || !w_uv || !k_nope || !v) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(kv_pages) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(k_nope) || !aligned16(v))
+    return MLA_ERR_INVALID_ARG;
+  if (chunk_start < 0 || chunk_start % p->chunk_tokens != 0) return MLA_ERR_INVALID_ARG;
+  DeviceInfo* dinfo = nullptr;
+  if ((st = extend_attrs(&dinfo))) return st;
+  ExpandArgs a;
+  dim3 grid;
+  if ((st = expand_setup(p, kv_pages, block_table, cache_seqlens, w_uk, w_uv, k_nope, v, dinfo->sm_count, &a, &grid)))
+    return st;
+  a.chunk_start = chunk_start;
+  return launch_expand(a, grid, stream);
+}
+
+int32_t mla_extend(const mla_extend_params* p, const void* q_nope, const void* q_rope, const void* kv_pages,
+                   const int32_t* block_table, const int32_t* cache_seqlens, const void* w_uk, const void* w_uv,
+                   float scale, void* out, float* lse, void* workspace, void* stream) {
+  int32_t st = check_extend(p);
+  if (st != MLA_OK) return st;
+  if (!q_nope || !q_rope || !kv_pages || !block_table || !cache_seqlens || !w_uk || !w_uv || !out || !lse ||
+      !workspace)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(kv_pages) || !aligned16(w_uk) || !aligned16(w_uv) ||
+      !aligned16(out) || !aligned16(lse) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MLA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return MLA_ERR_INVALID_ARG;
+  DeviceInfo* dinfo = nullptr;
+  if ((st = extend_attrs(&dinfo))) return st;
+  const ExtendLayout lay = extend_layout(p);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* kn = ws;
+  void* vv = ws + lay.kv;
+  float* acc_o = reinterpret_cast<float*>(ws + 2 * lay.kv);
+  float* acc_lse = reinterpret_cast<float*>(ws + 2 * lay.kv + lay.acc_o);
+  ExpandArgs ea;
+  dim3 eg;
+  if ((st = expand_setup(p, kv_pages, block_table, cache_seqlens, w_uk, w_uv, kn, vv, dinfo->sm_count, &ea, &eg)))
+    return st;
+  AttendArgs aa;
+  std::memset(&aa, 0, sizeof aa);
+  aa.map_kvc = ea.map_kvc;
+  if ((st = workspace_map(&aa.map_kn, kn, p)) || (st = workspace_map(&aa.map_v, vv, p))) return st;
+  aa.q_nope = static_cast<const __nv_bfloat16*>(q_nope);
+  aa.q_rope = static_cast<const __nv_bfloat16*>(q_rope);
+  aa.block_table = block_table;
+  aa.seqlens = cache_seqlens;
+  aa.acc_o = acc_o;
+  aa.acc_lse = acc_lse;
+  aa.out = static_cast<__nv_bfloat16*>(out);
+  aa.lse = lse;
+  aa.scale_log2 = scale * 1.4426950408889634f;
+  aa.B = p->batch;
+  aa.s_q = p->s_q;
+  aa.H = p->num_heads;
+  aa.C = p->chunk_tokens;
+  aa.max_pages_per_seq = p->max_pages_per_seq;
+  aa.timeout_ns = ea.timeout_ns;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((p->s_q + 127) / 128, p->num_heads, p->batch);
+  cfg.blockDim = dim3(kXThreads, 1, 1);
+  cfg.dynamicSmemBytes = kAtSmem;
+  pdl_config(&cfg, attr, stream);
+  const int n_chunks = (p->max_seqlen + p->chunk_tokens - 1) / p->chunk_tokens;
+  for (int k = 0; k < n_chunks; ++k) {
+    ea.chunk_start = aa.chunk_start = k * p->chunk_tokens;
+    if ((st = launch_expand(ea, eg, stream))) return st;
+    if (cudaLaunchKernelEx(&cfg, mla_attend_kernel, aa) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
 }
 
 int32_t mla_wait_selftest(int32_t timeout_us, void* stream) {

@@ -174,3 +174,39 @@ def first_sequences(w: Workload, batch: int) -> Workload:
     return dataclasses.replace(w, batch=b, seqlens=w.seqlens[:b].copy(), block_table=w.block_table[:b].copy(),
                                q_nope=w.q_nope[:b].copy(), q_rope=w.q_rope[:b].copy(),
                                meta=dict(w.meta, first_sequences=b))
+
+
+@dataclass
+class ExtendWorkload:
+    """Inputs of an extend by the expand path: the paged bf16 cache of `cache` (its last s_q rows
+    per sequence are the new tokens), the new tokens' non-absorbed queries and the per-head
+    up-projections (bf16 bit patterns)."""
+    cache: Workload
+    s_q: int
+    q_nope: np.ndarray   # uint16 [B, s_q, H, d_nope]
+    q_rope: np.ndarray   # uint16 [B, s_q, H, 64]
+    w_uk: np.ndarray     # uint16 [H, d_nope, 512]
+    w_uv: np.ndarray     # uint16 [H, 512, d_v]
+    scale: float
+
+
+def make_extend(seqlens, s_q: int, num_heads: int = 128, seed: int = 0, d_nope: int = 128, d_v: int = 128,
+                nan_tail: bool = True) -> ExtendWorkload:
+    """Seeded N(0, 1) cache and queries; W_UK and W_UV N(0, 1/512) so that expanded keys and values
+    are O(1).  nan_tail: cache rows past each sequence's end in its last page hold NaN."""
+    cache = make_custom(seqlens, num_heads=num_heads, s_q=1, seed=seed)
+    rng = np.random.default_rng(seed + 1)
+    B = cache.batch
+    if nan_tail:
+        for b in range(B):
+            L = int(cache.seqlens[b])
+            if L % PAGE:
+                cache.kv[cache.block_table[b, L // PAGE], L % PAGE:] = 0x7FC0
+    sd = 1.0 / math.sqrt(D_C)
+    return ExtendWorkload(
+        cache=cache, s_q=s_q,
+        q_nope=to_bf16_bits(rng.standard_normal((B, s_q, num_heads, d_nope), dtype=np.float32)),
+        q_rope=to_bf16_bits(rng.standard_normal((B, s_q, num_heads, D_R), dtype=np.float32)),
+        w_uk=to_bf16_bits((rng.standard_normal((num_heads, d_nope, D_C)) * sd).astype(np.float32)),
+        w_uv=to_bf16_bits((rng.standard_normal((num_heads, D_C, d_v)) * sd).astype(np.float32)),
+        scale=1.0 / math.sqrt(d_nope + D_R))

@@ -228,3 +228,34 @@ def test_head_projections_reject_bad_arguments_before_any_launch(lib):
         assert f(4, 128, 128, None, buf, buf, None) == _lib.MLA_ERR_INVALID_ARG        # null input
         assert f(4, 128, 128, buf, buf, odd, None) == _lib.MLA_ERR_INVALID_ARG         # misaligned output
         assert f(4, 128, 100, buf, buf, buf, None) == _lib.MLA_ERR_UNSUPPORTED         # width not a multiple of 64
+
+
+def test_extend_params_are_checked_without_a_gpu(lib):
+    """mla_extend_workspace_size validates the extend parameters on the host and sizes the
+    workspace: two bf16 [B][H][C][128] buffers and the float32 merge accumulators."""
+    ok = dict(batch=2, s_q=5, num_heads=16, num_pages=40, max_pages_per_seq=20, max_seqlen=1000, chunk_tokens=256)
+    p = _lib.MlaExtendParams.make(**ok)
+    n = ctypes.c_size_t()
+    assert lib.mla_extend_workspace_size(ctypes.byref(p), ctypes.byref(n)) == _lib.MLA_OK
+    a256 = lambda x: (x + 255) // 256 * 256
+    assert n.value == 2 * a256(2 * 16 * 256 * 128 * 2) + a256(2 * 5 * 16 * 128 * 4) + a256(2 * 5 * 16 * 4)
+    bad = [(dict(chunk_tokens=200), _lib.MLA_ERR_UNSUPPORTED),      # not a multiple of 128
+           (dict(d_v=64), _lib.MLA_ERR_UNSUPPORTED),               # only 128-wide heads
+           (dict(num_heads=256), _lib.MLA_ERR_UNSUPPORTED),
+           (dict(max_seqlen=20 * 64 + 1), _lib.MLA_ERR_INVALID_ARG),  # longer than the block table
+           (dict(s_q=1001), _lib.MLA_ERR_INVALID_ARG),             # more new tokens than rows
+           (dict(batch=0), _lib.MLA_ERR_INVALID_ARG),
+           (dict(page_size=32), _lib.MLA_ERR_UNSUPPORTED)]
+    for kw, status in bad:
+        q = _lib.MlaExtendParams.make(**{**ok, **kw})
+        assert lib.mla_extend_workspace_size(ctypes.byref(q), ctypes.byref(n)) == status, kw
+    q = _lib.MlaExtendParams.make(**ok)
+    q.reserved[2] = 1
+    assert lib.mla_extend_workspace_size(ctypes.byref(q), ctypes.byref(n)) == _lib.MLA_ERR_INVALID_ARG
+    buf = ctypes.c_void_p(256)
+    assert lib.mla_extend(ctypes.byref(p), buf, buf, buf, buf, buf, buf, buf, ctypes.c_float(0.1), buf, buf, None,
+                          None) == _lib.MLA_ERR_INVALID_ARG                       # no workspace
+    assert lib.mla_extend(ctypes.byref(p), buf, buf, buf, buf, buf, buf, buf, ctypes.c_float(0.0), buf, buf, buf,
+                          None) == _lib.MLA_ERR_INVALID_ARG                       # scale 0
+    assert lib.mla_expand_kv(ctypes.byref(p), buf, buf, buf, buf, buf, 100, buf, buf, None) == \
+        _lib.MLA_ERR_INVALID_ARG                                                  # chunk start not a chunk multiple

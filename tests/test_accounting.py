@@ -94,3 +94,10 @@ def test_algorithmic_totals_of_the_workloads():
     # bytes: each visible cache row once (1152 B bf16 / 656 B fp8), plus q, out, lse, block table, lengths
     b = bench.algorithmic_bytes([4096] * 32, 1, 128, 1152, 2)
     assert b == 32 * 4096 * 1152 + 32 * 128 * 576 * 2 + 32 * 128 * 512 * 2 + 32 * 128 * 4 + 32 * 64 * 4 + 32 * 4
+
+
+@pytest.mark.parametrize("row", golden()[1], ids=lambda r: r[0])
+def test_extend_flops_match_printed_path_one(row):
+    """bench.extend_flops (the extend leg's FLOP count) reproduces the printed path-one totals."""
+    name, q, k, p1, _ = row
+    assert close(bench.extend_flops(q, k, H) / 1e9, p1, 1), (name, bench.extend_flops(q, k, H) / 1e9, p1)
