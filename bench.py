@@ -95,10 +95,15 @@ def roofline_time_s(flops: int, nbytes: int, peaks) -> tuple[float, str]:
     return (t_b, "hbm") if t_b >= t_f else (t_f, "tensor")
 
 
+DECODE_SOURCES = ("common.cuh", "decode_kernel.cuh", "plan.h", "ptx.cuh")
+
+
 def kernel_source_hash() -> str:
+    """Hash of the sources the decode kernel is compiled from (its device code and the planner
+    whose metadata it walks); DRAM counters taken with other sources are not reported."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "mla_absorbed_decode_02_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
+    for name in DECODE_SOURCES:
         with open(os.path.join(d, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -267,12 +272,13 @@ def _device_inputs(w, dev):
     return host, {k: v.to(dev) for k, v in host.items()}
 
 
-def _params(w):
+def _params(w, token_group=0):
     from mla_absorbed_decode_02_gb300 import (MlaDecodeParams, MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_OUT_BF16,
                                               MLA_OUT_F32)
     return MlaDecodeParams.make(w.batch, w.s_q, w.num_heads, w.num_pages, w.block_table.shape[1], causal=w.causal,
                                 kv_dtype=MLA_KV_FP8_E4M3 if w.kv_dtype == "fp8" else MLA_KV_BF16,
-                                out_dtype=MLA_OUT_F32 if w.out_dtype == "f32" else MLA_OUT_BF16)
+                                out_dtype=MLA_OUT_F32 if w.out_dtype == "f32" else MLA_OUT_BF16,
+                                token_group=token_group)
 
 
 def _accounting(w, peaks):
@@ -300,7 +306,7 @@ def _roofline(w, name, peaks, t_dec):
     return roof
 
 
-def time_workload(w, name, peaks, steps, warmup, dev, flush, dist=None):
+def time_workload(w, name, peaks, steps, warmup, dev, flush, dist=None, token_group=0):
     """Device timing of one workload, inputs resident in HBM, L2 flushed before every step.
 
     Pass 1 times whole steps (decode kernel + LSE combine, nothing between the two launches, so
@@ -311,7 +317,7 @@ def time_workload(w, name, peaks, steps, warmup, dev, flush, dist=None):
     from mla_absorbed_decode_02_gb300 import (Decoder, mla_combine, mla_decode_splitkv, mla_device_error,
                                               mla_get_scheduler_metadata)
     host, d = _device_inputs(w, dev)
-    p = _params(w)
+    p = _params(w, token_group)
     dec = Decoder(p, dev)
     out, lse = dec.new_outputs()
     stream = torch.cuda.current_stream(dev)
@@ -469,7 +475,7 @@ def run_ours(args, w, peaks, world, rank, local):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    r = time_workload(w, args.workload, peaks, args.steps, args.warmup, dev, flush, dist)
+    r = time_workload(w, args.workload, peaks, args.steps, args.warmup, dev, flush, dist, args.token_group)
     clk = clocks.stop()
     t_step, t_dec = r["t_step"], r["t_dec"]
     t_max = reduce_max(t_step, dist, dev)
@@ -522,7 +528,7 @@ def run_ours(args, w, peaks, world, rank, local):
         "config": {"workload": args.workload + (f" (first {w.batch} sequences)" if args.batch else ""),
                    "batch": w.batch, "heads": w.num_heads, "s_q": w.s_q,
                    "seqlens": f"{int(w.seqlens.min())}..{int(w.seqlens.max())} (sum {int(w.seqlens.sum())})",
-                   "kv_dtype": w.kv_dtype, "pages": w.num_pages, "units": units,
+                   "kv_dtype": w.kv_dtype, "pages": w.num_pages, "units": units, "token_group": args.token_group or 1,
                    "l2": "flushed before every step (256 MiB write)", "parallelism": f"replicas x{n}",
                    "timing": f"median of {args.steps} steps after {args.warmup} warm-up steps, CUDA events"},
         "tflops": n * flops / t_max / 1e12, "kv_gbs": n * kv_bytes(w.seqlens, row_bytes) / t_max / 1e9,
@@ -549,17 +555,22 @@ def run_ours(args, w, peaks, world, rank, local):
         clocks = ClockSampler(local)
         clocks.start()
         time.sleep(0.3)
-        for name in ("uniform4k", "long", "fp8_mtp2"):
-            if name == args.workload:
+        # (fp8_mtp2 twice: one CTA pair per new token, and both new tokens of a sequence on shared
+        # pages, token group 2, which reads the cache once)
+        for name, grp in (("uniform4k", 0), ("long", 0), ("fp8_mtp2", 0), ("fp8_mtp2", 2)):
+            if name == args.workload and grp == args.token_group:
                 continue
             wk = mw.make_workload(WORKLOAD_INDEX[name])
-            rk = time_workload(wk, name, peaks, args.steps, args.warmup, dev, flush)
+            rk = time_workload(wk, name, peaks, args.steps, args.warmup, dev, flush, token_group=grp)
             _, _, _, tr, _ = _accounting(wk, peaks)
-            per[name] = {"value": 100.0 * tr / rk["t_step"], "ms_per_step": rk["t_step"] * 1e3,
-                         "kernel_ms": rk["t_dec"] * 1e3, "roofline": _roofline(wk, name, peaks, rk["t_dec"]),
-                         "config": {"batch": wk.batch, "s_q": wk.s_q, "kv_dtype": wk.kv_dtype,
-                                    "seqlens": f"{int(wk.seqlens.min())}..{int(wk.seqlens.max())} "
-                                               f"(sum {int(wk.seqlens.sum())})"}}
+            per[name + (f"_token_group{grp}" if grp else "")] = {
+                "value": 100.0 * tr / rk["t_step"], "ms_per_step": rk["t_step"] * 1e3,
+                "kernel_ms": rk["t_dec"] * 1e3,
+                "roofline": _roofline(wk, name + (f"_token_group{grp}" if grp else ""), peaks, rk["t_dec"]),
+                "config": {"batch": wk.batch, "s_q": wk.s_q, "kv_dtype": wk.kv_dtype, "units": rk["dec"].num_units,
+                           "token_group": grp or 1,
+                           "seqlens": f"{int(wk.seqlens.min())}..{int(wk.seqlens.max())} "
+                                      f"(sum {int(wk.seqlens.sum())})"}}
             del rk, wk
             torch.cuda.empty_cache()
         per_clk = clocks.stop()
@@ -579,6 +590,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="time the chosen workload only")
     ap.add_argument("--no-extend", action="store_true", help="skip the extend (expand path) timing")
+    ap.add_argument("--token-group", type=int, default=0,
+                    help="new tokens per work block for the chosen workload (mla_decode_params.token_group)")
     ap.add_argument("--batch", type=int, default=0,
                     help="keep only the first B sequences of the workload (same recipe; for profiling small cases)")
     args = ap.parse_args()

@@ -83,9 +83,15 @@ typedef struct mla_decode_params {
                                 zero => every new token sees all L_b keys */
   int32_t kv_dtype;          /* mla_kv_dtype */
   int32_t out_dtype;         /* mla_out_dtype */
-  int32_t num_units;         /* work units (one 2-SM cluster each); 0 = as many as fit at once */
+  int32_t num_units;         /* work units (one cluster of 2G SMs each, G = the token group); 0 = as
+                                many as fit at once */
   int32_t timeout_us;        /* limit of every bounded wait inside the kernels; 0 = 2,000,000 us */
-  int32_t reserved[5];       /* must be zero */
+  int32_t token_group;       /* G: new tokens of a sequence decoded together on shared pages: each page
+                                is read from memory once for the G tokens (one CTA pair per token, a
+                                cluster of 2G CTAs, pages multicast to every pair); 1..4 and dividing
+                                s_q; 0 = 1.  Clusters of 4 / 8 CTAs occupy 144 / 120 of GB300's 152 SMs,
+                                so G > 1 pays where DRAM, not the SMs, bounds the decode */
+  int32_t reserved[4];       /* must be zero */
 } mla_decode_params;
 
 /*
@@ -156,10 +162,12 @@ int32_t mla_combine(const mla_decode_params* p, void* out, float* lse, const voi
  * num_units must be >= 1; sched must hold sched_bytes for that unit count.
  * Layout of sched (int32): [0] = 0x4D4C4131, [1] = units, [2] = B*s_q query blocks,
  * [3] = partial slots used, [4] = per-unit budget of work positions (one per 64-key
- * tile plus a fixed cost per query block; diagnostic), [5..7] = 0; then per unit 8
- * ints {qb_begin, tile_begin, qb_end, tile_end (exclusive), first_split, 0, 0, 0}
- * (qb_begin = -1: no work); then num_splits[B*s_q]; then split_offset[B*s_q].  A query
- * block qb = b*s_q + t.
+ * tile plus a fixed cost per work block; diagnostic), [5] = G, the token group,
+ * [6..7] = 0; then per unit 8 ints {wb_begin, tile_begin, wb_end, tile_end (exclusive),
+ * first_split, 0, 0, 0} (wb_begin = -1: no work); then num_splits[B*s_q]; then
+ * split_offset[B*s_q].  A query block qb = b*s_q + t; a work block wb holds the G query
+ * blocks wb*G .. wb*G + G - 1 (G = 1: wb = qb), and its tiles are those of its last
+ * token; num_splits is the same for the G query blocks of a work block.
  * Returns MLA_ERR_INVALID_ARG for a negative length, or for lengths whose work
  * positions exceed 2^31 - 1 in total (sched then holds a header without the magic
  * word).  The scheduler kernel (mla_get_scheduler_metadata) reports the same two

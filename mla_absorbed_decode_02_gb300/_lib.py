@@ -39,13 +39,13 @@ class MlaDecodeParams(ctypes.Structure):
                 ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("max_pages_per_seq", ctypes.c_int32), ("causal", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("num_units", ctypes.c_int32), ("timeout_us", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 5)]
+                ("token_group", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
 
     @classmethod
     def make(cls, batch, s_q, num_heads, num_pages, max_pages_per_seq, causal=True, kv_dtype=MLA_KV_BF16,
-             out_dtype=MLA_OUT_BF16, num_units=0, timeout_us=0, page_size=64):
+             out_dtype=MLA_OUT_BF16, num_units=0, timeout_us=0, page_size=64, token_group=0):
         return cls(batch, s_q, num_heads, num_pages, page_size, max_pages_per_seq, int(bool(causal)), kv_dtype,
-                   out_dtype, num_units, timeout_us)
+                   out_dtype, num_units, timeout_us, token_group)
 
 
 class MlaExtendParams(ctypes.Structure):

@@ -91,6 +91,7 @@ struct DecodeArgs {
   float* lse_acc;        // [slots][H]
   float scale_log2;      // softmax scale * log2(e)
   int32_t H, s_q, causal, max_pages, out_f32, num_units, num_qb, kv_fp8;
+  int32_t group;         // G: new tokens per work block; a unit is a cluster of 2G CTAs, one pair per token
   uint64_t timeout_ns;
 };
 

@@ -108,7 +108,8 @@ enum : uint32_t {
   B_X_FREE = B_X_FULL + 2,          // [parity] the peer consumed what this CTA sent for tile t
   B_ML = B_X_FREE + 2,              // [parity] running max / row sum of tile t published
   B_TI_FULL = B_ML + 2,             // [t mod 8] tile-schedule entry of tile t published
-  kNumBars = B_TI_FULL + kTiRing
+  B_KV_SHARED = B_TI_FULL + kTiRing, // + stage: (token groups, loading CTA) every pair's PV(t) done
+  kNumBars = B_KV_SHARED + kStages
 };
 constexpr uint32_t OFF_TMEM_SLOT = kNumBars * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
@@ -119,18 +120,21 @@ struct Piece {
   int qb, t0, t1, split;
 };
 
-// Walks the pieces (query block, tile range) of one unit record.
+// Walks the pieces (query block, tile range) of one unit record.  The record's ranges are over
+// work blocks of `group` tokens; this CTA pair's token is `g` of each block, so its query block
+// is blk * group + g, over the block's tiles (a token before the block's last may see none of
+// the last one or two).
 struct PieceWalker {
   const int32_t* seqlens;
-  int s_q, causal, first_qb, qb, qb_end, tile_begin, tile_end, first_split;
+  int s_q, causal, group, g, first_qb, qb, qb_end, tile_begin, tile_end, first_split;
   __device__ bool next(Piece& p) {
     while (qb <= qb_end) {
       const int cur = qb++;
-      const int nt = num_tiles(visible_keys(seqlens[cur / s_q], s_q, cur % s_q, causal));
+      const int nt = block_tiles(seqlens, s_q, causal, group, cur);
       const int a = (cur == first_qb) ? tile_begin : 0;
       const int b = (cur == qb_end) ? tile_end : nt;
       if (nt > 0 && a < b) {
-        p.qb = cur;
+        p.qb = cur * group + g;
         p.t0 = a;
         p.t1 = b;
         p.split = (cur == first_qb) ? first_split : 0;
@@ -340,8 +344,11 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t base = smem_addr(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t half = cluster_ctarank(), peer = half ^ 1;
-  const int unit = blockIdx.x >> 1;
+  // a unit is a cluster of 2G CTAs: pair g (ranks 2g, 2g + 1) decodes token g of each work block,
+  // the two CTAs of a pair own the two halves of the latent dims
+  const uint32_t rank = cluster_ctarank(), half = rank & 1, peer = rank ^ 1;
+  const int grp = args.group, g = (int)(rank >> 1);
+  const int unit = blockIdx.x / (2 * grp);
 
   auto bar = [&](uint32_t i) { return base + SM_BAR + 8 * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_BAR + OFF_ABORT);
@@ -368,6 +375,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
       mbar_init(bar(B_ML + p), 4);
     }
     for (int i = 0; i < kTiRing; ++i) mbar_init(bar(B_TI_FULL + i), 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(bar(B_KV_SHARED + s), grp);  // one PV commit per pair
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -396,7 +404,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
   pdl_wait_prerequisites();
   // ---- unit record (uniform across the cluster); bail out early on bad metadata
   const int32_t* sched = args.sched;
-  const bool bad_meta = sched[0] != kSchedMagic || sched[1] != args.num_units || sched[2] != args.num_qb;
+  const bool bad_meta = sched[0] != kSchedMagic || sched[1] != args.num_units || sched[2] != args.num_qb ||
+                        sched[5] != grp;
   const int32_t* rec = sched + kSchedHeader + kUnitInts * unit;
   if (bad_meta || rec[0] < 0) {  // bad metadata, or no work for this unit (both CTAs take this path)
     if (bad_meta && tid == 0) atomicCAS(&g_mla_error, 0, 5);
@@ -416,12 +425,15 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
   walker0.seqlens = args.seqlens;
   walker0.s_q = args.s_q;
   walker0.causal = args.causal;
+  walker0.group = grp;
+  walker0.g = g;
   walker0.qb = rec[0];
   walker0.first_qb = rec[0];
   walker0.tile_begin = rec[1];
   walker0.qb_end = rec[2];
   walker0.tile_end = rec[3];
   walker0.first_split = rec[4];
+  const int first_qb = rec[0] * grp + g;  // this pair's query block of the unit's first work block
 
   if (warp == 0) {
     // ================================================================ TMA producer
@@ -444,6 +456,28 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           tma_load_2d(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 512 + 32 * half, page * 64, pol_kv);
         }
       };
+      // Token groups: pair 0 loads each page half once into the same half of every pair
+      // (multicast); the other pairs only expect the bytes on their own barrier.
+      const uint16_t mc_mask = (uint16_t)(0x5555u & ((1u << (2 * grp)) - 1u)) << half;
+      auto load_page_group = [&](uint32_t st, int page) {
+        const uint32_t sbase = base + st * kStageBytes;
+        if (kFp8) {
+          mbar_arrive_expect_tx(bar(B_KV_FULL + st), kFp8StageTx);
+          if (g != 0) return;
+          tma_load_2d_mc(sbase + kStageCodes, &args.map_kvc, bar(B_KV_FULL + st), 256 * half, page * 64, mc_mask, pol_kv);
+          tma_load_2d_mc(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 528 + 64 * half, page * 64, mc_mask,
+                         pol_kv);
+          tma_load_2d_mc(sbase + kStageScales, &args.map_kvs, bar(B_KV_FULL + st), 512, page * 64, mc_mask, pol_kv);
+        } else {
+          mbar_arrive_expect_tx(bar(B_KV_FULL + st), kBf16StageTx);
+          if (g != 0) return;
+          for (int blk = 0; blk < 4; ++blk)
+            tma_load_2d_mc(sbase + blk * kLatBlock, &args.map_kvc, bar(B_KV_FULL + st), 256 * half + 64 * blk,
+                           page * 64, mc_mask, pol_kv);
+          tma_load_2d_mc(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 512 + 32 * half, page * 64, mc_mask,
+                         pol_kv);
+        }
+      };
       // logical page lp of sequence b; a length beyond the block table is reported, and no entry
       // past the row is read
       auto page_of = [&](int b, int lp) {
@@ -457,8 +491,11 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
       // non-empty.  That page and the block's RoPE-query half go out straight from the unit
       // record, before the walk over the lengths.
       mbar_arrive_expect_tx(bar(B_QR_FULL), 8192);
-      tma_load_3d(base + SM_QR, &args.map_qr, bar(B_QR_FULL), 32 * half, 0, walker0.first_qb, pol_q);
-      load_page(0, page_of(walker0.first_qb / args.s_q, walker0.tile_begin));
+      tma_load_3d(base + SM_QR, &args.map_qr, bar(B_QR_FULL), 32 * half, 0, first_qb, pol_q);
+      if (grp == 1)
+        load_page(0, page_of(first_qb / args.s_q, walker0.tile_begin));
+      else
+        load_page_group(0, page_of(first_qb / args.s_q, walker0.tile_begin));
       TileCursor cur;
       cur.init(walker0);
       TileInfo ti;
@@ -478,7 +515,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           next_qb = ahead.next(np) ? np.qb : -1;
         }
         const uint32_t st = t % kStages, ph = (t / kStages) & 1;
-        if (t > 0 && !wait_one(bar(B_KV_EMPTY + st), ph ^ 1, wc, kSiteKvEmpty)) break;
+        // the stage is free: here (this CTA's PV of its last tile), or, for the loading pair of a
+        // token group, in every pair
+        if (t > 0 && !wait_one(bar((grp > 1 && g == 0 ? B_KV_SHARED : B_KV_EMPTY) + st), ph ^ 1, wc, kSiteKvEmpty))
+          break;
         {  // the tile's schedule entry for the softmax warpgroups
           const uint32_t e = base + SM_TI + (t % kTiRing) * 32;
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(e), "r"(ti.qb), "r"(ti.valid), "r"(ti.split),
@@ -491,9 +531,19 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           prev_qb = ti.qb;
           prev_split = ti.split;
         }
-        if (t > 0) load_page(st, page_of(ti.qb / args.s_q, ti.tile));  // (tile 0's page went out above)
+        if (t > 0) {  // (tile 0's page went out above)
+          if (grp == 1)
+            load_page(st, page_of(ti.qb / args.s_q, ti.tile));
+          else
+            load_page_group(st, page_of(ti.qb / args.s_q, ti.tile));
+        }
         ++t;
       }
+      // Token groups: the loading pair's CTAs receive every pair's last PV commits; they stay
+      // until those arrived (the barrier phases of the last min(t, stages) tiles).
+      if (grp > 1 && g == 0 && !*abort_flag)
+        for (uint32_t k = t > kStages ? t - kStages : 0; k < t; ++k)
+          if (!wait_one(bar(B_KV_SHARED + k % kStages), (k / kStages) & 1, wc, kSiteKvEmpty)) break;
     }
   } else if (warp == 1 || warp == 3) {
     // ================================================================ MMA issuers
@@ -546,6 +596,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
             mma_bf16_ss(tmem + TM_O, a, bv, id_pv, (!ti.first || k > 0) ? 1u : 0u);
           }
           mma_commit(bar(B_KV_EMPTY + st));
+          if (grp > 1) mma_commit_mc(bar(B_KV_SHARED + st), (uint16_t)(1u << half));  // the loading CTA
           mma_commit(bar(B_P_FREE + pb));
           ++t;
         }
@@ -658,7 +709,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
     auto epilogue = [&](float m_fin, float l_tot, int part, int nparts) {
       const bool split = num_splits[epi_qb] > 1;
       const int slot = split ? split_offset[epi_qb] + epi_split : 0;
-      const float inv_l = 1.f / l_tot;
+      const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;  // a token that saw no key: out = 0, lse = -inf
       if (split || args.out_f32) {
         float* dst = (split ? args.o_acc + (int64_t)slot * H * 512 : reinterpret_cast<float*>(args.out) + (int64_t)epi_qb * H * 512) +
                      256 * half + 4 * chk;
@@ -734,7 +785,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
       tc_fence_before();
     };
 
-    if (w == 0) load_q_tmem(walker0.first_qb);  // piece 0's query half (the planner makes piece 0 non-empty)
+    if (w == 0) load_q_tmem(first_qb);  // piece 0's query half (the planner makes piece 0 non-empty)
     int np_qb = -1;  // query block of the piece after the current tile's (from the schedule)
 
     float l_mine = 0.f, m_ref = 0.f;  // this warpgroup's part of the row sum, relative to m_ref
@@ -905,7 +956,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           }
           float m = m_prev, alpha = 1.f;
           if (kFull && x.first) {
-            m = cm;  // finite: token 0 of a piece's first tile is visible
+            // finite unless this token sees no key of the tile (a token before the last of a group,
+            // on the group's last tile): then any finite value, the tile's P is zero
+            m = cm > -INFINITY ? cm : 0.f;
           } else if (cm > m_prev + 8.f) {
             m = cm;
             alpha = exp2f(m_prev - cm);
@@ -979,9 +1032,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           if (kFull && valid < kTileTok) {
             // rows past the sequence end must not reach the PV product (0 * garbage): zero them
             const uint32_t sbase = base + (t % kStages) * kStageBytes;
-            const int nz = (kTileTok - valid) * 4 * 8;  // 16-byte chunks: rows x 4 blocks x 8
+            const int v0 = valid > 0 ? valid : 0;
+            const int nz = (kTileTok - v0) * 4 * 8;  // 16-byte chunks: rows x 4 blocks x 8
             for (int idx = r; idx < nz; idx += kRows) {
-              const int row = valid + idx / 32, blk = (idx / 8) & 3, ch = idx & 7;
+              const int row = v0 + idx / 32, blk = (idx / 8) & 3, ch = idx & 7;
               asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(sbase + blk * kLatBlock + row * 128 + ch * 16),
                            "r"(0u));
             }
@@ -1005,7 +1059,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
         asm volatile("prefetch.global.L2 [%0];" ::"l"(qr));
       }
       // (the lean instance first: it is the one the loop runs back to back)
-      if (__builtin_expect(!(x.first || x.last), 1)) {
+      if (__builtin_expect(!(x.first || x.last || x.valid < kTileTok), 1)) {
         if (!tile(std::false_type{})) {
           ok = false;
           break;
@@ -1063,11 +1117,11 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
   }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     mla_decode_bf16_kernel(const __grid_constant__ DecodeArgs args) {
   decode_body<false>(args);
 }
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     mla_decode_fp8_kernel(const __grid_constant__ DecodeArgs args) {
   decode_body<true>(args);
 }

@@ -20,19 +20,19 @@ namespace mla {
 
 // ----------------------------------------------------------------- split planner (device twin)
 // One CTA of 1024 threads runs the planner phases of plan.h (the prefix sums on one thread).
-__global__ void __launch_bounds__(1024) mla_sched_kernel(const int32_t* seqlens, int B, int s_q, int causal, int U,
-                                                         int32_t* sched) {
+__global__ void __launch_bounds__(1024) mla_sched_kernel(const int32_t* seqlens, int B, int s_q, int causal, int G,
+                                                         int U, int32_t* sched) {
   __shared__ int64_t sh_total;
-  const int NQB = B * s_q, tid = threadIdx.x, nt = blockDim.x;
+  const int NQB = B * s_q, NWB = NQB / G, tid = threadIdx.x, nt = blockDim.x;
   int32_t* units = sched + kSchedHeader;
   int32_t* num_splits = units + kUnitInts * U;
-  int32_t* pos = num_splits + NQB;  // scratch until the last phase
-  plan_phase_cost(seqlens, s_q, causal, NQB, pos, tid, nt);
+  int32_t* pos = num_splits + NQB;  // scratch until the last phase (one entry per work block)
+  plan_phase_cost(seqlens, s_q, causal, G, NWB, pos, tid, nt);
   // a negative length is outside the contract: reported, and planned as an empty sequence
   for (int b = tid; b < B; b += nt)
     if (seqlens[b] < 0) atomicCAS(&g_mla_error, 0, MLA_ERR_INVALID_ARG);
   __syncthreads();
-  if (tid == 0) sh_total = plan_phase_scan(pos, NQB);
+  if (tid == 0) sh_total = plan_phase_scan(pos, NWB);
   __syncthreads();
   if (sh_total > kMaxPlanPositions) {  // more work positions than an int32 holds: refuse the plan
     if (tid == 0) {
@@ -42,10 +42,10 @@ __global__ void __launch_bounds__(1024) mla_sched_kernel(const int32_t* seqlens,
     return;
   }
   const int64_t total = sh_total, Bq = plan_budget(total, U);
-  plan_phase_units(seqlens, s_q, causal, NQB, pos, total, Bq, U, units, tid, nt);
-  plan_phase_splits(seqlens, s_q, causal, NQB, pos, Bq, num_splits, tid, nt);
+  plan_phase_units(seqlens, s_q, causal, G, NWB, pos, total, Bq, U, units, tid, nt);
+  plan_phase_splits(seqlens, s_q, causal, G, NWB, pos, Bq, num_splits, tid, nt);
   __syncthreads();
-  if (tid == 0) plan_phase_finish(NQB, U, Bq, sched);
+  if (tid == 0) plan_phase_finish(NQB, U, G, Bq, sched);
 }
 
 // ----------------------------------------------------------------- LSE combine of split partials
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const int32_t* sched, 
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float wk = expf(wgt[k] - L);
+        const float wk = L > -INFINITY ? expf(wgt[k] - L) : 0.f;  // every split empty: out = 0
 #pragma unroll
         for (int f = 0; f < kNf; ++f) {
           acc[f].x += wk * v[k][f].x;
@@ -225,7 +225,7 @@ using namespace mla;
 struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
-  int max_clusters = 0;
+  int max_clusters[5] = {0, 0, 0, 0, 0};  // [G]: clusters of 2G decode CTAs that fit at once
 };
 std::mutex g_mu;
 DeviceInfo g_dev[64];
@@ -243,21 +243,23 @@ int32_t device_info(DeviceInfo** out) {
         cudaFuncSetAttribute(mla_decode_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
             cudaSuccess)
       return MLA_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (d.sm_count / 2), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, (void*)mla_decode_bf16_kernel, &cfg) != cudaSuccess || n <= 0)
-      n = d.sm_count / 2;
-    d.max_clusters = n;
+    for (int G = 1; G <= 4; ++G) {  // GPCs hold whole clusters: bigger ones leave SMs idle
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * G * (d.sm_count / (2 * G)), 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = kSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2 * G;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, (void*)mla_decode_bf16_kernel, &cfg) != cudaSuccess || n <= 0)
+        n = d.sm_count / (2 * G);
+      d.max_clusters[G] = n;
+    }
     if (!g_encode) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -277,14 +279,22 @@ int32_t check_params(const mla_decode_params* p) {
   if (!p) return MLA_ERR_INVALID_ARG;
   if (p->batch < 1 || p->num_heads < 1 || p->num_pages < 1 || p->max_pages_per_seq < 1) return MLA_ERR_INVALID_ARG;
   if (p->s_q < 1 || p->page_size < 1 || p->num_units < 0 || p->timeout_us < 0) return MLA_ERR_INVALID_ARG;
-  for (int i = 0; i < 5; ++i)
+  for (int i = 0; i < 4; ++i)
     if (p->reserved[i] != 0) return MLA_ERR_INVALID_ARG;
+  if (p->token_group < 0 || p->token_group > 4 || (p->token_group > 0 && p->s_q % p->token_group != 0))
+    return MLA_ERR_INVALID_ARG;
   if (p->kv_dtype != MLA_KV_BF16 && p->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
   if (p->out_dtype != MLA_OUT_BF16 && p->out_dtype != MLA_OUT_F32) return MLA_ERR_INVALID_ARG;
   if (p->page_size != 64 || p->s_q > 8 || p->num_heads > 128) return MLA_ERR_UNSUPPORTED;
   if ((int64_t)p->batch * p->s_q > (1 << 24) || (int64_t)p->num_pages * 64 > INT32_MAX) return MLA_ERR_UNSUPPORTED;
   return MLA_OK;
 }
+
+// New tokens per work block: the caller's token_group, else 1.  A group of G tokens reads each
+// page once instead of G times, but GPCs hold whole clusters: clusters of 4 CTAs fill 144 of
+// the 152 SMs, of 8 CTAs 120, so where the decode is bound by the SMs' work rather than by
+// DRAM (every s_q >= 2 workload measured) the per-token mode is the faster one.
+int resolve_group(const mla_decode_params* p) { return p->token_group > 0 ? p->token_group : 1; }
 
 int32_t resolve_units(const mla_decode_params* p, int32_t* U) {
   if (p->num_units > 0) {
@@ -294,8 +304,14 @@ int32_t resolve_units(const mla_decode_params* p, int32_t* U) {
   DeviceInfo* d = nullptr;
   int32_t st = device_info(&d);
   if (st != MLA_OK) return st;
-  *U = d->max_clusters;
+  *U = d->max_clusters[resolve_group(p)];
   return MLA_OK;
+}
+
+// Split-partial slots: each unit boundary splits at most one work block, and each split block
+// takes one slot per split for each of its G query blocks.
+size_t partial_slots(const mla_decode_params* p, int32_t U) {
+  return (size_t)p->batch * p->s_q + (size_t)resolve_group(p) * U;
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
@@ -430,7 +446,7 @@ int32_t mla_get_workspace_size(const mla_decode_params* p, size_t* sched_bytes, 
   if ((st = resolve_units(p, &U)) != MLA_OK) return st;
   const int64_t nqb = (int64_t)p->batch * p->s_q;
   *sched_bytes = sizeof(int32_t) * (size_t)sched_ints(U, (int)nqb);
-  const size_t slots = (size_t)(nqb + U);
+  const size_t slots = partial_slots(p, U);
   *workspace_bytes = align256(slots * p->num_heads * 512 * sizeof(float)) + align256(slots * p->num_heads * sizeof(float));
   return MLA_OK;
 }
@@ -441,7 +457,8 @@ int32_t mla_plan_host(const mla_decode_params* p, int32_t num_units, const int32
   if (num_units < 1 || !cache_seqlens || !sched) return MLA_ERR_INVALID_ARG;
   for (int b = 0; b < p->batch; ++b)
     if (cache_seqlens[b] < 0) return MLA_ERR_INVALID_ARG;
-  return plan_units(cache_seqlens, p->batch, p->s_q, p->causal != 0, num_units, static_cast<int32_t*>(sched))
+  return plan_units(cache_seqlens, p->batch, p->s_q, p->causal != 0, resolve_group(p), num_units,
+                    static_cast<int32_t*>(sched))
              ? MLA_OK
              : MLA_ERR_INVALID_ARG;
 }
@@ -453,8 +470,8 @@ int32_t mla_get_scheduler_metadata(const mla_decode_params* p, const int32_t* ca
   if (!cache_seqlens || !sched) return MLA_ERR_INVALID_ARG;
   int32_t U = 0;
   if ((st = resolve_units(p, &U)) != MLA_OK) return st;
-  mla_sched_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(cache_seqlens, p->batch, p->s_q,
-                                                                      p->causal != 0, U, static_cast<int32_t*>(sched));
+  mla_sched_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(
+      cache_seqlens, p->batch, p->s_q, p->causal != 0, resolve_group(p), U, static_cast<int32_t*>(sched));
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -471,8 +488,8 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
   if ((st = device_info(&dinfo)) != MLA_OK) return st;
   int32_t U = 0;
   if ((st = resolve_units(p, &U)) != MLA_OK) return st;
-  const int H = p->num_heads, NQB = p->batch * p->s_q;
-  const size_t slots = (size_t)NQB + U;
+  const int H = p->num_heads, NQB = p->batch * p->s_q, G = resolve_group(p);
+  const size_t slots = partial_slots(p, U);
 
   DecodeArgs a;
   std::memset(&a, 0, sizeof a);
@@ -500,21 +517,26 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
   a.out_f32 = p->out_dtype == MLA_OUT_F32;
   a.num_units = U;
   a.num_qb = NQB;
+  a.group = G;
   a.timeout_ns = (uint64_t)(p->timeout_us > 0 ? p->timeout_us : 2000000) * 1000ull;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * U, 1, 1);
+  cfg.gridDim = dim3(2 * G * U, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  // cluster shape from __cluster_dims__; programmatic dependent launch: the kernel's set-up
+  // one unit = a cluster of 2G CTAs; programmatic dependent launch: the kernel's set-up
   // (barriers, tensor memory) overlaps the end of the kernel before it in the stream, and it
   // waits (griddepcontrol.wait) before reading any global memory
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2 * G;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const cudaError_t e = a.kv_fp8 ? cudaLaunchKernelEx(&cfg, mla_decode_fp8_kernel, a)
                                  : cudaLaunchKernelEx(&cfg, mla_decode_bf16_kernel, a);
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
@@ -530,7 +552,7 @@ int32_t mla_combine(const mla_decode_params* p, void* out, float* lse, const voi
   int32_t U = 0;
   if ((st = resolve_units(p, &U)) != MLA_OK) return st;
   const int H = p->num_heads, NQB = p->batch * p->s_q;
-  const size_t slots = (size_t)NQB + U;
+  const size_t slots = partial_slots(p, U);
   const float* o_acc = static_cast<const float*>(workspace);
   const float* lse_acc =
       reinterpret_cast<const float*>(static_cast<const char*>(workspace) + align256(slots * H * 512 * sizeof(float)));

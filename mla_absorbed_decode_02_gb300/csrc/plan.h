@@ -1,5 +1,8 @@
-// Split-KV planner: assigns contiguous stretches of (query block, 64-token tile)
-// work to units (one 2-SM cluster each), splitting long sequences across units.
+// Split-KV planner: assigns contiguous stretches of (work block, 64-token tile)
+// work to units, splitting long sequences across units.  A work block is a group
+// of G consecutive new tokens of one sequence (G = 1: one query block; G > 1: the
+// G tokens share every page, one CTA pair per token in a cluster of 2G CTAs); its
+// tiles are those of its last token, which sees the most keys.
 // The same function runs in the scheduler kernel (one thread) and on the host
 // (mla_plan_host), so the CPU tests exercise exactly the device algorithm.
 //
@@ -44,11 +47,18 @@ MLA_HD inline int32_t visible_keys(int32_t L, int s_q, int t, int causal) {
 
 MLA_HD inline int32_t num_tiles(int32_t visible) { return (visible + kTile - 1) / kTile; }
 
+// Tiles of work block blk (tokens blk*G .. blk*G + G - 1 of the flattened [B][s_q] order):
+// those of its last token.
+MLA_HD inline int32_t block_tiles(const int32_t* seqlens, int s_q, int causal, int G, int blk) {
+  const int qb_last = blk * G + G - 1;
+  return num_tiles(visible_keys(seqlens[qb_last / s_q], s_q, qb_last % s_q, causal));
+}
+
 MLA_HD inline int64_t sched_ints(int num_units, int num_qb) {
   return kSchedHeader + (int64_t)kUnitInts * num_units + 2 * (int64_t)num_qb;
 }
 
-// Work positions.  Query blocks are laid out one after another on a line of
+// Work positions.  Work blocks are laid out one after another on a line of
 // cost units: block qb occupies [pos[qb], pos[qb] + kPieceFixedCost + nt[qb]),
 // its first kPieceFixedCost units standing for the per-piece overhead and then
 // one unit per 64-token tile (tile t at pos[qb] + kPieceFixedCost + t).  With
@@ -56,11 +66,12 @@ MLA_HD inline int64_t sched_ints(int num_units, int num_qb) {
 // [u*B, (u+1)*B).  Everything below follows in closed form, so the device runs
 // each phase in parallel (the prefix sums on one thread).
 //
-// Phase 1 (per query block): nt[qb] and cost; written into num_splits[] as scratch.
-MLA_HD inline void plan_phase_cost(const int32_t* seqlens, int s_q, int causal, int NQB, int32_t* cost, int begin,
-                                   int stride) {
+// Phase 1 (per work block): nt[qb] and cost.  (In this and the next phases qb indexes work
+// blocks, NQB counts them.)
+MLA_HD inline void plan_phase_cost(const int32_t* seqlens, int s_q, int causal, int G, int NQB, int32_t* cost,
+                                   int begin, int stride) {
   for (int qb = begin; qb < NQB; qb += stride) {
-    const int32_t nt = num_tiles(visible_keys(seqlens[qb / s_q], s_q, qb % s_q, causal));
+    const int32_t nt = block_tiles(seqlens, s_q, causal, G, qb);
     cost[qb] = nt > 0 ? nt + kPieceFixedCost : 0;
   }
 }
@@ -86,7 +97,7 @@ MLA_HD inline int64_t plan_budget(int64_t total, int U) {
 }
 
 // Phase 3 (per unit): the unit record.  pos[] = block start positions.
-MLA_HD inline void plan_phase_units(const int32_t* seqlens, int s_q, int causal, int NQB, const int32_t* pos,
+MLA_HD inline void plan_phase_units(const int32_t* seqlens, int s_q, int causal, int G, int NQB, const int32_t* pos,
                                     int64_t total, int64_t B, int U, int32_t* units, int begin, int stride) {
   for (int u = begin; u < U; u += stride) {
     int32_t* rec = units + kUnitInts * u;
@@ -98,13 +109,13 @@ MLA_HD inline void plan_phase_units(const int32_t* seqlens, int s_q, int causal,
     int a = 0, b = NQB;
     while (a < b) {
       const int m = (a + b) / 2;
-      const int32_t nt = num_tiles(visible_keys(seqlens[m / s_q], s_q, m % s_q, causal));
+      const int32_t nt = block_tiles(seqlens, s_q, causal, G, m);
       const int64_t last = (int64_t)pos[m] + kPieceFixedCost + nt - 1;
       if (nt > 0 && last >= lo) b = m; else if (nt == 0 && (int64_t)pos[m] > lo) b = m; else a = m + 1;
     }
     // skip empty blocks
     int qb0 = a;
-    while (qb0 < NQB && num_tiles(visible_keys(seqlens[qb0 / s_q], s_q, qb0 % s_q, causal)) == 0) ++qb0;
+    while (qb0 < NQB && block_tiles(seqlens, s_q, causal, G, qb0) == 0) ++qb0;
     if (qb0 >= NQB) continue;
     const int64_t first0 = (int64_t)pos[qb0] + kPieceFixedCost;
     if (first0 >= hi) continue;  // the range holds only overhead positions
@@ -116,8 +127,8 @@ MLA_HD inline void plan_phase_units(const int32_t* seqlens, int s_q, int causal,
       if ((int64_t)pos[m] + kPieceFixedCost < hi) a = m; else b = m;
     }
     int qb1 = a;
-    while (qb1 > qb0 && num_tiles(visible_keys(seqlens[qb1 / s_q], s_q, qb1 % s_q, causal)) == 0) --qb1;
-    const int32_t nt1 = num_tiles(visible_keys(seqlens[qb1 / s_q], s_q, qb1 % s_q, causal));
+    while (qb1 > qb0 && block_tiles(seqlens, s_q, causal, G, qb1) == 0) --qb1;
+    const int32_t nt1 = block_tiles(seqlens, s_q, causal, G, qb1);
     const int64_t t_begin = lo - first0 > 0 ? lo - first0 : 0;
     int64_t t_end = hi - ((int64_t)pos[qb1] + kPieceFixedCost);
     if (t_end > nt1) t_end = nt1;
@@ -130,22 +141,23 @@ MLA_HD inline void plan_phase_units(const int32_t* seqlens, int s_q, int causal,
   }
 }
 
-// Phase 4 (per query block): number of units its tiles span.
-MLA_HD inline void plan_phase_splits(const int32_t* seqlens, int s_q, int causal, int NQB, const int32_t* pos,
+// Phase 4 (per work block): number of units its tiles span, written for each of its G query
+// blocks (num_splits is indexed by query block).
+MLA_HD inline void plan_phase_splits(const int32_t* seqlens, int s_q, int causal, int G, int NQB, const int32_t* pos,
                                      int64_t B, int32_t* num_splits, int begin, int stride) {
   for (int qb = begin; qb < NQB; qb += stride) {
-    const int32_t nt = num_tiles(visible_keys(seqlens[qb / s_q], s_q, qb % s_q, causal));
-    if (nt == 0) {
-      num_splits[qb] = 0;
-      continue;
+    const int32_t nt = block_tiles(seqlens, s_q, causal, G, qb);
+    int32_t n = 0;
+    if (nt > 0) {
+      const int64_t first = (int64_t)pos[qb] + kPieceFixedCost;
+      n = (int32_t)((first + nt - 1) / B - first / B + 1);
     }
-    const int64_t first = (int64_t)pos[qb] + kPieceFixedCost;
-    num_splits[qb] = (int32_t)((first + nt - 1) / B - first / B + 1);
+    for (int g = 0; g < G; ++g) num_splits[qb * G + g] = n;
   }
 }
 
-// Phase 5 (one thread): slots of the split partials; header.
-MLA_HD inline void plan_phase_finish(int NQB, int U, int64_t B, int32_t* sched) {
+// Phase 5 (one thread): slots of the split partials (per query block); header.
+MLA_HD inline void plan_phase_finish(int NQB, int U, int G, int64_t B, int32_t* sched) {
   int32_t* num_splits = sched + kSchedHeader + kUnitInts * U;
   int32_t* split_offset = num_splits + NQB;
   int32_t slots = 0;
@@ -158,7 +170,8 @@ MLA_HD inline void plan_phase_finish(int NQB, int U, int64_t B, int32_t* sched) 
   sched[2] = NQB;
   sched[3] = slots;
   sched[4] = (int32_t)B;  // per-unit budget of positions (diagnostic)
-  sched[5] = sched[6] = sched[7] = 0;
+  sched[5] = G;           // tokens per work block
+  sched[6] = sched[7] = 0;
 }
 
 // A refused plan: a header without the magic word, which the decode and combine kernels
@@ -169,23 +182,23 @@ MLA_HD inline void plan_refuse(int32_t* sched) {
 
 // Host twin: all phases in order, one "thread".  The split_offset region of
 // sched serves as scratch for the block positions until phase 5 fills it.
-// Returns false (and writes a refused header) when the lengths need more cost
-// positions than an int32 holds.
-MLA_HD inline bool plan_units(const int32_t* seqlens, int B_, int s_q, int causal, int U, int32_t* sched) {
-  const int NQB = B_ * s_q;
+// G divides s_q.  Returns false (and writes a refused header) when the lengths
+// need more cost positions than an int32 holds.
+MLA_HD inline bool plan_units(const int32_t* seqlens, int B_, int s_q, int causal, int G, int U, int32_t* sched) {
+  const int NQB = B_ * s_q, NWB = NQB / G;
   int32_t* units = sched + kSchedHeader;
   int32_t* num_splits = units + kUnitInts * U;
   int32_t* pos = num_splits + NQB;
-  plan_phase_cost(seqlens, s_q, causal, NQB, pos, 0, 1);
-  const int64_t total = plan_phase_scan(pos, NQB);
+  plan_phase_cost(seqlens, s_q, causal, G, NWB, pos, 0, 1);
+  const int64_t total = plan_phase_scan(pos, NWB);
   if (total > kMaxPlanPositions) {
     plan_refuse(sched);
     return false;
   }
   const int64_t B = plan_budget(total, U);
-  plan_phase_units(seqlens, s_q, causal, NQB, pos, total, B, U, units, 0, 1);
-  plan_phase_splits(seqlens, s_q, causal, NQB, pos, B, num_splits, 0, 1);
-  plan_phase_finish(NQB, U, B, sched);
+  plan_phase_units(seqlens, s_q, causal, G, NWB, pos, total, B, U, units, 0, 1);
+  plan_phase_splits(seqlens, s_q, causal, G, NWB, pos, B, num_splits, 0, 1);
+  plan_phase_finish(NQB, U, G, B, sched);
   return true;
 }
 

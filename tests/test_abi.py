@@ -62,6 +62,9 @@ def test_workspace_size_without_gpu(lib):
     (dict(kv_dtype=7), _lib.MLA_ERR_INVALID_ARG),
     (dict(out_dtype=5), _lib.MLA_ERR_INVALID_ARG),
     (dict(num_units=-1), _lib.MLA_ERR_INVALID_ARG),
+    (dict(s_q=2, token_group=3), _lib.MLA_ERR_INVALID_ARG),   # must divide s_q
+    (dict(s_q=8, token_group=8), _lib.MLA_ERR_INVALID_ARG),   # at most 4 (clusters of 8 CTAs)
+    (dict(token_group=-1), _lib.MLA_ERR_INVALID_ARG),
 ])
 def test_bad_params_are_rejected(lib, kw, status):
     with pytest.raises(_lib.MlaError) as e:
@@ -73,6 +76,17 @@ def test_null_pointers_rejected_before_any_launch(lib):
     with pytest.raises(_lib.MlaError) as e:
         _lib.mla_decode(_p(), None, None, None, None, None, 0.07, None, None, None, None, stream=0)
     assert e.value.status == _lib.MLA_ERR_INVALID_ARG
+
+
+def test_workspace_of_a_token_group(lib):
+    """A token group of G takes G partial slots for each unit boundary."""
+    _, wb = _lib.mla_get_workspace_size(_p(batch=3, s_q=4, num_units=7, token_group=2))
+    slots = 12 + 2 * 7
+    assert wb == _a256(slots * 128 * 512 * 4) + _a256(slots * 128 * 4)
+
+
+def _a256(x):
+    return (x + 255) // 256 * 256
 
 
 def test_reserved_must_be_zero(lib):
@@ -95,27 +109,34 @@ def visible(L, s_q, t, causal):
 
 
 def decode_plan(sched, B, s_q, causal, seqlens):
-    """Expand the metadata into the list of pieces (unit, qb, t0, t1, split_idx)."""
-    U, nqb = sched[1], sched[2]
-    assert sched[0] == _lib.SCHED_MAGIC and nqb == B * s_q
+    """Expand the metadata into the list of pieces (unit, qb, t0, t1, split_idx).  The unit
+    records range over work blocks of G = sched[5] tokens whose tiles are their last token's;
+    each work block's piece is one piece of each of its G query blocks.  Returns ntiles per
+    query block as the tiles its work block covers."""
+    U, nqb, G = sched[1], sched[2], sched[5]
+    assert sched[0] == _lib.SCHED_MAGIC and nqb == B * s_q and G >= 1 and s_q % G == 0
     units = sched[8:8 + 8 * U].reshape(U, 8)
     num_splits = sched[8 + 8 * U:8 + 8 * U + nqb]
     offsets = sched[8 + 8 * U + nqb:]
-    ntiles = [-(-visible(seqlens[q // s_q], s_q, q % s_q, causal) // TILE) for q in range(nqb)]
+    own = [-(-visible(seqlens[q // s_q], s_q, q % s_q, causal) // TILE) for q in range(nqb)]
+    wtiles = [own[w * G + G - 1] for w in range(nqb // G)]   # a work block: its last token's tiles
+    assert all(own[w * G + g] <= wtiles[w] for w in range(nqb // G) for g in range(G))
+    ntiles = [wtiles[q // G] for q in range(nqb)]
     pieces = []
     for u in range(U):
-        qb0, tb, qb1, te, fs = units[u, :5]
-        if qb0 < 0:
+        wb0, tb, wb1, te, fs = units[u, :5]
+        if wb0 < 0:
             continue
-        for qb in range(qb0, qb1 + 1):
-            a = tb if qb == qb0 else 0
-            b = te if qb == qb1 else ntiles[qb]
-            if ntiles[qb] > 0 and a < b:
-                pieces.append((u, qb, a, b, fs if qb == qb0 else 0))
+        for wb in range(wb0, wb1 + 1):
+            a = tb if wb == wb0 else 0
+            b = te if wb == wb1 else wtiles[wb]
+            if wtiles[wb] > 0 and a < b:
+                for g in range(G):
+                    pieces.append((u, wb * G + g, a, b, fs if wb == wb0 else 0))
     return pieces, ntiles, num_splits, offsets
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(16))
 def test_plan_covers_every_tile_once(lib, seed):
     rng = np.random.default_rng(seed)
     B = int(rng.integers(1, 80))
@@ -132,7 +153,8 @@ def test_plan_covers_every_tile_once(lib, seed):
         seqlens = rng.choice([0, 1, 2, 127, 128, 129, 65536], size=B)
     seqlens = seqlens.astype(np.int32)
     U = int(rng.choice([1, 2, 3, 7, 19, 76, 148, 500]))
-    p = MlaDecodeParams.make(B, s_q, 128, 100, 10, causal=causal, num_units=U)
+    group = [0, 1, *[g for g in (2, 3, 4) if s_q % g == 0]][seed % (2 + sum(s_q % g == 0 for g in (2, 3, 4)))]
+    p = MlaDecodeParams.make(B, s_q, 128, 100, 10, causal=causal, num_units=U, token_group=group)
     sched = _lib.mla_plan_host(p, U, seqlens)
     pieces, ntiles, num_splits, offsets = decode_plan(sched, B, s_q, causal, seqlens)
     # every tile of every query block exactly once, pieces non-empty
@@ -144,7 +166,7 @@ def test_plan_covers_every_tile_once(lib, seed):
             seen[(qb, t)] = u
     assert len(seen) == sum(ntiles)
     # units hold contiguous, increasing stretches of (qb, tile)
-    order = [(qb, a) for _, qb, a, _, _ in pieces]
+    order = [(qb // sched[5], a, qb) for _, qb, a, _, _ in pieces]
     assert order == sorted(order)
     # split bookkeeping: split indices 0..n-1 per query block, slots disjoint
     per_qb = {}
@@ -160,7 +182,9 @@ def test_plan_covers_every_tile_once(lib, seed):
                 s = offsets[qb] + i
                 assert s not in slots
                 slots.add(s)
-    assert sched[3] == len(slots) <= B * s_q + U
+    G = sched[5]
+    assert G == (group or 1)
+    assert sched[3] == len(slots) <= B * s_q + G * U
 
 
 def test_plan_balances_load(lib):

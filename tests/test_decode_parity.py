@@ -26,8 +26,8 @@ def built():
     build()
 
 
-def full_check(w, tol=BF16_TOL, num_units=0, what=""):
-    out, lse, _ = run_gpu(w, num_units=num_units)
+def full_check(w, tol=BF16_TOL, num_units=0, what="", token_group=0):
+    out, lse, _ = run_gpu(w, num_units=num_units, token_group=token_group)
     ref_out, ref_lse = oracle_full(w, threads=THREADS)
     return compare(out, lse, ref_out, ref_lse, tol, what or w.name, out_bf16=w.out_dtype == "bf16")
 
@@ -106,6 +106,32 @@ def test_up_to_eight_new_tokens(s_q, causal):
     Sequences shorter than s_q leave the first causal tokens with no visible key."""
     w = mw.make_custom([1, 3, 8, 9, 65, 300, 1000], num_heads=128, s_q=s_q, causal=causal, seed=40 + s_q)
     full_check(w, num_units=5, what=f"s_q={s_q} causal={causal}")
+
+
+@pytest.mark.parametrize("s_q,group,kv", [(2, 1, "bf16"), (2, 2, "bf16"), (4, 2, "bf16"), (4, 4, "bf16"),
+                                           (6, 3, "bf16"), (2, 2, "fp8"), (4, 4, "fp8")])
+@pytest.mark.parametrize("num_units", [1, 3, 40])
+def test_token_groups(s_q, group, kv, num_units):
+    """G new tokens of a sequence decoded together, each page loaded once into the G CTA pairs
+    of a cluster.  Lengths 64k + 1 .. 64k + G - 1 put keys only the later tokens see on the work
+    block's last tile (for the earlier tokens a fully masked tile, at 40 units often a piece of
+    its own); sequences shorter than s_q leave early tokens no key at all; one is empty."""
+    w = mw.make_custom([0, 1, 3, 65, 66, 129, 130, 640, 701], num_heads=64, s_q=s_q, causal=True, kv_dtype=kv,
+                       seed=60 + 7 * s_q + group)
+    full_check(w, tol=FP8_TOL if kv == "fp8" else BF16_TOL, num_units=num_units, token_group=group,
+               what=f"s_q={s_q} G={group} {kv} units={num_units}")
+
+
+def test_token_group_plan_on_the_device_matches_the_host():
+    import torch
+    from mla_absorbed_decode_02_gb300 import Decoder, mla_plan_host
+    w = mw.make_workload(4)
+    _, _, _, _, seq = to_device(w)
+    dec = Decoder(params_for(w, token_group=2))
+    dec.plan(seq)
+    torch.cuda.synchronize()
+    host = mla_plan_host(params_for(w, num_units=dec.num_units, token_group=2), dec.num_units, w.seqlens)
+    assert host[5] == 2 and np.array_equal(dec.sched.cpu().numpy(), host)
 
 
 def test_fp8_cache_four_new_tokens():
