@@ -338,7 +338,7 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 
 // The kernel body, instantiated once per cache format (no code of the other format in the
 // instruction stream of either).
-template <bool kFp8>
+template <bool kFp8, bool kGroups>
 __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -347,7 +347,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
   // a unit is a cluster of 2G CTAs: pair g (ranks 2g, 2g + 1) decodes token g of each work block,
   // the two CTAs of a pair own the two halves of the latent dims
   const uint32_t rank = cluster_ctarank(), half = rank & 1, peer = rank ^ 1;
-  const int grp = args.group, g = (int)(rank >> 1);
+  const int grp = kGroups ? args.group : 1, g = kGroups ? (int)(rank >> 1) : 0;
   const int unit = blockIdx.x / (2 * grp);
 
   auto bar = [&](uint32_t i) { return base + SM_BAR + 8 * i; };
@@ -958,7 +958,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           if (kFull && x.first) {
             // finite unless this token sees no key of the tile (a token before the last of a group,
             // on the group's last tile): then any finite value, the tile's P is zero
-            m = cm > -INFINITY ? cm : 0.f;
+            m = (!kGroups || cm > -INFINITY) ? cm : 0.f;
           } else if (cm > m_prev + 8.f) {
             m = cm;
             alpha = exp2f(m_prev - cm);
@@ -1059,7 +1059,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
         asm volatile("prefetch.global.L2 [%0];" ::"l"(qr));
       }
       // (the lean instance first: it is the one the loop runs back to back)
-      if (__builtin_expect(!(x.first || x.last || x.valid < kTileTok), 1)) {
+      if (__builtin_expect(!(x.first || x.last || (kGroups && x.valid < kTileTok)), 1)) {
         if (!tile(std::false_type{})) {
           ok = false;
           break;
@@ -1117,13 +1117,23 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
   }
 }
 
+// One pair per new token (clusters of 2 CTAs) and token groups (clusters of 2G CTAs, G > 1) are
+// separate instances: the grouped code costs the per-token kernel registers.
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_bf16_kernel(const __grid_constant__ DecodeArgs args) {
-  decode_body<false>(args);
+  decode_body<false, false>(args);
 }
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_fp8_kernel(const __grid_constant__ DecodeArgs args) {
-  decode_body<true>(args);
+  decode_body<true, false>(args);
+}
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_decode_bf16_group_kernel(const __grid_constant__ DecodeArgs args) {
+  decode_body<false, true>(args);
+}
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_decode_fp8_group_kernel(const __grid_constant__ DecodeArgs args) {
+  decode_body<true, true>(args);
 }
 
 }  // namespace mla

@@ -238,11 +238,10 @@ int32_t device_info(DeviceInfo** out) {
   DeviceInfo& d = g_dev[dev];
   if (!d.ready) {
     if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
-    if (cudaFuncSetAttribute(mla_decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(mla_decode_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess)
-      return MLA_ERR_CUDA;
+    for (const void* k : {(const void*)mla_decode_bf16_kernel, (const void*)mla_decode_fp8_kernel,
+                          (const void*)mla_decode_bf16_group_kernel, (const void*)mla_decode_fp8_group_kernel})
+      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+        return MLA_ERR_CUDA;
     for (int G = 1; G <= 4; ++G) {  // GPCs hold whole clusters: bigger ones leave SMs idle
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * G * (d.sm_count / (2 * G)), 1, 1);
@@ -537,8 +536,10 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = a.kv_fp8 ? cudaLaunchKernelEx(&cfg, mla_decode_fp8_kernel, a)
-                                 : cudaLaunchKernelEx(&cfg, mla_decode_bf16_kernel, a);
+  const cudaError_t e = G > 1 ? (a.kv_fp8 ? cudaLaunchKernelEx(&cfg, mla_decode_fp8_group_kernel, a)
+                                          : cudaLaunchKernelEx(&cfg, mla_decode_bf16_group_kernel, a))
+                               : (a.kv_fp8 ? cudaLaunchKernelEx(&cfg, mla_decode_fp8_kernel, a)
+                                           : cudaLaunchKernelEx(&cfg, mla_decode_bf16_kernel, a));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
