@@ -64,14 +64,16 @@ __global__ void __launch_bounds__(kXThreads, 1) mla_expand_kernel(const __grid_c
   const uint32_t C_FULL = bars + 8 * (2 * kExRing);
   auto A_FULL = [&](int i) { return bars + 8 * (2 * kExRing + 1 + i); };
   auto A_EMPTY = [&](int i) { return bars + 8 * (2 * kExRing + 3 + i); };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kExCBytes + kExRing * kExStage + 8 * 16);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kExCBytes + kExRing * kExStage + 8 * 16 + 8);
+  constexpr int kNumBars = 2 * kExRing + 5;
+  static_assert(8 * kNumBars + 16 <= 256, "expansion barrier area");
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kExCBytes + kExRing * kExStage + 8 * kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kExCBytes + kExRing * kExStage + 8 * kNumBars + 8);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.y, h0 = blockIdx.z * args.heads_per_cta, nh = args.heads_per_cta;
   const int rel0 = blockIdx.x * 128, j0 = args.chunk_start + rel0;
 
   if (tid == 0) {
-    for (int i = 0; i < 2 * kExRing + 5; ++i) mbar_init(bars + 8 * i, (i >= 2 * kExRing + 3) ? 4 : 1);
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bars + 8 * i, (i >= 2 * kExRing + 3) ? 4 : 1);
     *abort_flag = 0;
     prefetch_tensormap(&args.map_kvc);
     prefetch_tensormap(&args.map_wuk);
@@ -232,14 +234,16 @@ __global__ void __launch_bounds__(kXThreads, 1) mla_attend_kernel(const __grid_c
   auto S_FREE = [&](int i) { return bars + 8 * (2 * kAtRing + 3 + i); };
   auto P_FULL = [&](int i) { return bars + 8 * (2 * kAtRing + 5 + i); };
   auto PV_DONE = [&](int i) { return bars + 8 * (2 * kAtRing + 7 + i); };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAtRing * kAtStage + 2 * kAtP + 8 * 20);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kAtRing * kAtStage + 2 * kAtP + 8 * 20 + 8);
+  constexpr int kNumBars = 2 * kAtRing + 9;
+  static_assert(8 * kNumBars + 16 <= 256, "attention barrier area");
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAtRing * kAtStage + 2 * kAtP + 8 * kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kAtRing * kAtStage + 2 * kAtP + 8 * kNumBars + 8);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * 128, h = blockIdx.y, b = blockIdx.z;
   const int s_q = args.s_q, H = args.H;
 
   if (tid == 0) {
-    for (int i = 0; i < 2 * kAtRing + 9; ++i) {
+    for (int i = 0; i < kNumBars; ++i) {
       const int k = i - 2 * kAtRing;  // Q full, S free and P full take one arrive per row warp
       mbar_init(bars + 8 * i, (k == 0 || (k >= 3 && k <= 6)) ? 4 : 1);
     }
