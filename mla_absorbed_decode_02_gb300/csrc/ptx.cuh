@@ -110,14 +110,6 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* 
       "l"(map), "r"(bar), "r"(x), "r"(y), "h"(cta_mask), "l"(policy)
       : "memory");
 }
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z,
-                                               uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
-      " [%0], [%1, {%3, %4, %5}], [%2], %6, %7;" ::"r"(dst),
-      "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(cta_mask), "l"(policy)
-      : "memory");
-}
 // 16-byte global store with an L2 eviction-priority hint.
 __device__ __forceinline__ void st_global_v4_hint(void* ptr, float4 v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "f"(v.x), "f"(v.y), "f"(v.z),
