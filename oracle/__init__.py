@@ -196,7 +196,7 @@ def absorb_query(q_nope, w_uk) -> np.ndarray:
     in float64.  q_nope [..., H, d_nope], w_uk [H, d_nope, d_c] -> [..., H, d_c]."""
     q = np.asarray(q_nope, np.float64)
     w = np.asarray(w_uk, np.float64)
-    return np.einsum("...hk,hkn->...hn", q, w)
+    return np.einsum("...hk,hkn->...hn", q, w, optimize=True)
 
 
 def project_output(o_latent, w_uv) -> np.ndarray:
@@ -204,7 +204,7 @@ def project_output(o_latent, w_uv) -> np.ndarray:
     section), in float64.  o_latent [..., H, d_c], w_uv [H, d_c, d_v] -> [..., H, d_v]."""
     o = np.asarray(o_latent, np.float64)
     w = np.asarray(w_uv, np.float64)
-    return np.einsum("...hk,hkn->...hn", o, w)
+    return np.einsum("...hk,hkn->...hn", o, w, optimize=True)
 
 
 # ---------------------------------------------------------------- the expand path (extend)
@@ -232,8 +232,8 @@ def expand_kv(c, w_uk, w_uv):
     W_UV [H, d_c, d_v] (the layouts of absorb_query / project_output).
     c [L, d_c] -> (k^N [H, L, d_nope], v [H, L, d_v]), float64."""
     c = np.asarray(c, np.float64)
-    return (np.einsum("hnc,jc->hjn", np.asarray(w_uk, np.float64), c),
-            np.einsum("jc,hcv->hjv", c, np.asarray(w_uv, np.float64)))
+    return (np.einsum("hnc,jc->hjn", np.asarray(w_uk, np.float64), c, optimize=True),
+            np.einsum("jc,hcv->hjv", c, np.asarray(w_uv, np.float64), optimize=True))
 
 
 def extend_expanded(q_nope, q_rope, kv_bits, block_table, seqlens, w_uk, w_uv, scale, page_size=64,
@@ -258,12 +258,13 @@ def extend_expanded(q_nope, q_rope, kv_bits, block_table, seqlens, w_uk, w_uv, s
         kn, v = expand_kv(rows[:, :d_c], w_uk, w_uv)
         if round_kv:
             kn, v = round_bf16(kn), round_bf16(v)
-        s = scale * (np.einsum("thn,hjn->thj", q_nope[b], kn) + np.einsum("thr,jr->thj", q_rope[b], rows[:, d_c:]))
+        s = scale * (np.einsum("thn,hjn->thj", q_nope[b], kn, optimize=True) +
+                     np.einsum("thr,jr->thj", q_rope[b], rows[:, d_c:], optimize=True))
         hidden = np.arange(L)[None, :] > (L - s_q + np.arange(s_q))[:, None]      # [s_q, L]
         s[np.broadcast_to(hidden[:, None, :], s.shape)] = -np.inf
         m = s.max(axis=-1, keepdims=True)
         e = np.exp(s - m)
         l = e.sum(axis=-1)
-        out[b] = np.einsum("thj,hjv->thv", e / l[..., None], v)
+        out[b] = np.einsum("thj,hjv->thv", e / l[..., None], v, optimize=True)
         lse[b] = m[..., 0] + np.log(l)
     return out, lse
