@@ -172,3 +172,17 @@ def test_single_token_extend_equals_absorbed_decode_then_projection():
     dl = float(np.abs(lse_x - lse_d.cpu().numpy()).max())
     print(f"[parity] expand path vs absorbed path on the GPU: rel L2 {rel:.3g}, max |d lse| {dl:.3g}")
     assert rel <= 1e-2 and dl <= 5e-3
+
+
+def test_extend_full_size_sampled_heads():
+    """The bench's extend workload (one sequence, 512 new tokens after a 32,768-row prefix, 128
+    heads, chunks of 4096 rows: nine chunks merged), run in full; the oracle computes a sample of
+    heads spread over the four 32-row lane quarters, every new token."""
+    x = mw.make_extend([32768 + 512], s_q=512, num_heads=128, seed=11, nan_tail=False)
+    out, lse = run_extend(x, 4096)
+    heads = np.array([0, 37, 70, 127])
+    sub = mw.ExtendWorkload(cache=x.cache, s_q=x.s_q, q_nope=x.q_nope[:, :, heads], q_rope=x.q_rope[:, :, heads],
+                            w_uk=x.w_uk[heads], w_uv=x.w_uv[heads], scale=x.scale)
+    ref_out, ref_lse = oracle_extend(sub, round_kv=True)
+    compare(out[:, :, heads], lse[:, :, heads], ref_out, ref_lse, BF16_TOL, "extend 512 after 32K, sampled heads",
+            out_bf16=True)
