@@ -122,6 +122,14 @@ def test_token_groups(s_q, group, kv, num_units):
                what=f"s_q={s_q} G={group} {kv} units={num_units}")
 
 
+@pytest.mark.parametrize("group,causal", [(2, True), (4, True), (4, False), (2, False)])
+def test_token_groups_of_eight_new_tokens(group, causal):
+    """s_q = 8 in work blocks of 2 or 4 tokens (several blocks per sequence, each read once by
+    its cluster), causal and not."""
+    w = mw.make_custom([1, 8, 9, 66, 300, 1000], num_heads=128, s_q=8, causal=causal, seed=80 + group)
+    full_check(w, num_units=7, token_group=group, what=f"s_q=8 G={group} causal={causal}")
+
+
 def test_token_group_plan_on_the_device_matches_the_host():
     import torch
     from mla_absorbed_decode_02_gb300 import Decoder, mla_plan_host
