@@ -499,6 +499,13 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
       TileCursor cur;
       cur.init(walker0);
       TileInfo ti;
+      // bf16 cache: the block-table entry of the next tile is read one iteration ahead, so its
+      // latency overlaps the wait for a free stage (ragged decode 117.4 against 119.5 us; the FP8
+      // kernel measured 1% slower with it and reads the entry when it needs it)
+      TileCursor la = cur;
+      TileInfo tl;
+      int pg_next = -1;
+      if (!kFp8 && la.next(tl) && la.next(tl)) pg_next = page_of(tl.qb / args.s_q, tl.tile);  // tile 1
       PieceWalker ahead = walker0;  // one piece ahead of the tile walk
       Piece np;
       ahead.next(np);  // piece 0
@@ -532,10 +539,12 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           prev_split = ti.split;
         }
         if (t > 0) {  // (tile 0's page went out above)
+          const int page = kFp8 ? page_of(ti.qb / args.s_q, ti.tile) : pg_next;
           if (grp == 1)
-            load_page(st, page_of(ti.qb / args.s_q, ti.tile));
+            load_page(st, page);
           else
-            load_page_group(st, page_of(ti.qb / args.s_q, ti.tile));
+            load_page_group(st, page);
+          if (!kFp8 && la.next(tl)) pg_next = page_of(tl.qb / args.s_q, tl.tile);
         }
         ++t;
       }
