@@ -9,7 +9,9 @@
 //   mla_expand_kernel  K^N[b][h][j] = W_UK[h] c_j and V[b][h][j] = c_j W_UV[h] for the chunk's
 //                      rows (bf16, zero rows past the sequence's end), one tcgen05 GEMM per
 //                      (128 rows, head): the rows' latent tile stays in shared memory while
-//                      the heads' weights stream through it.
+//                      the heads' weights stream through it, two 64-deep chunks per TMA box.
+// Boxes are large on purpose: one thread issuing TMA copies spends about the same time per
+// copy (~0.23 us) whatever its size, so fewer, bigger boxes move more bytes per SM.
 //   mla_attend_kernel  per (128 new tokens, head, sequence): S = [q^N, q^R] . [K^N, k^R]^T,
 //                      causal mask, online softmax, O += P V over the chunk's 64-key tiles,
 //                      then the LSE merge with the result of the chunks before it (float32
@@ -20,25 +22,35 @@
 
 namespace mla {
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z,
+                                            int w, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy)
+      : "memory");
+}
+
 constexpr int kXThreads = 192;                    // warp 0: TMA, warp 1: MMA, warps 2..5: row work
 constexpr int kXDim = 128;                        // d_nope = d_v
 constexpr uint32_t kXBox = 64 * 128;              // [64 rows][64 bf16], 128-byte swizzle: 8 KB
 
 // ---------------------------------------------------------------- expansion
-constexpr int kExRing = 5;                        // weight chunks in flight
+constexpr int kExRing = 3;                        // weight stages in flight (two 64-deep chunks each)
 constexpr uint32_t kExCBytes = 16 * kXBox;        // latent tile: 128 rows x 512 dims (8 chunks of 16 KB)
-constexpr uint32_t kExStage = 2 * kXBox;          // one 64-deep chunk of W_UK[h] or W_UV[h]: 16 KB
+constexpr uint32_t kExStage = 4 * kXBox;          // two 64-deep chunks of W_UK[h] or W_UV[h]: 32 KB, one box
 constexpr uint32_t kExSmem = 1024 + kExCBytes + kExRing * kExStage + 256;
 
 struct ExpandArgs {
   CUtensorMap map_kvc;  // cache rows: bf16 {576, num_pages * 64}, box {64, 64}, 128-byte swizzle
-  CUtensorMap map_wuk;  // W_UK: bf16 {512, 128, H}, box {64, 128, 1}, 128-byte swizzle
-  CUtensorMap map_wuv;  // W_UV: bf16 {128, 512, H}, box {64, 64, 1}, 128-byte swizzle
+  CUtensorMap map_wuk;  // W_UK: bf16 {64 k, 128 n, 8 k-chunks (128 B apart), H}, box {64, 128, 2, 1}, 128-byte swizzle
+  CUtensorMap map_wuv;  // W_UV: bf16 {64 n, 512 k, 2 n-blocks (128 B apart), H}, box {64, 128, 2, 1}, 128-byte swizzle
   const int32_t* block_table;
   const int32_t* seqlens;
-  __nv_bfloat16* kn;    // [B][H][C][128]
-  __nv_bfloat16* v;     // [B][H][C][128]
+  __nv_bfloat16* kn;    // [B][H][C][ld] (first 128 of each row)
+  __nv_bfloat16* v;     // [B][H][C][ld]
   int32_t B, H, C, chunk_start, heads_per_cta, s_q, max_pages_per_seq;
+  int32_t ld;           // row stride of kn and v, elements: 128 (separate buffers) or 256 (K^N | V rows)
   uint64_t timeout_ns;
 };
 
@@ -96,7 +108,7 @@ __global__ void __launch_bounds__(kXThreads, 1) mla_expand_kernel(const __grid_c
   wc.abort_local = abort_flag;
   wc.abort_peer = 0;
   wc.timeout_ns = args.timeout_ns;
-  const int n_it = nh * 16;  // per head: 8 chunks of W_UK[h], then 8 of W_UV[h]
+  const int n_it = nh * 8;  // per head: 4 stages of W_UK[h], then 4 of W_UV[h]
   if (active && warp == 0 && lane == 0) {
     const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
     // the 128 rows' latent tile: two pages (the second clamped to the first past the end)
@@ -108,16 +120,14 @@ __global__ void __launch_bounds__(kXThreads, 1) mla_expand_kernel(const __grid_c
       tma_load_2d(c_base + k * 2 * kXBox + kXBox, &args.map_kvc, C_FULL, 64 * k, p1 * 64, stream);
     }
     for (int it = 0; it < n_it; ++it) {
-      const int st = it % kExRing, h = h0 + it / 16, part = (it >> 3) & 1, k = it & 7;
+      const int st = it % kExRing, h = h0 + it / 8, part = (it >> 2) & 1, kp = it & 3;
       if (it >= kExRing && !wait_one(W_EMPTY(st), ((it / kExRing) - 1) & 1, wc, kSiteKvEmpty)) break;
       const uint32_t sb = ring + st * kExStage;
       mbar_arrive_expect_tx(W_FULL(st), kExStage);
-      if (part == 0) {
-        tma_load_3d(sb, &args.map_wuk, W_FULL(st), 64 * k, 0, h, keep);
-      } else {
-        tma_load_3d(sb, &args.map_wuv, W_FULL(st), 0, 64 * k, h, keep);
-        tma_load_3d(sb + kXBox, &args.map_wuv, W_FULL(st), 64, 64 * k, h, keep);
-      }
+      if (part == 0)  // W_UK[h] chunks 2kp, 2kp + 1: [chunk][128 n][64 k]
+        tma_load_4d(sb, &args.map_wuk, W_FULL(st), 0, 0, 2 * kp, h, keep);
+      else            // W_UV[h] rows 128 kp .. 128 kp + 127: [n block][128 k][64 n]
+        tma_load_4d(sb, &args.map_wuv, W_FULL(st), 0, 128 * kp, 0, h, keep);
     }
   } else if (active && warp == 1 && lane == 0) {
     const uint32_t idesc_k = idesc_bf16_f32(128, 128, 0, 0), idesc_v = idesc_bf16_f32(128, 128, 0, 1);
@@ -128,18 +138,19 @@ __global__ void __launch_bounds__(kXThreads, 1) mla_expand_kernel(const __grid_c
       tc_fence_after();
       for (int part = 0; part < 2 && ok; ++part) {
         const uint32_t d = tmem + buf * 256 + part * 128;
-        for (int k = 0; k < 8; ++k) {
-          const int it = hi * 16 + part * 8 + k, st = it % kExRing;
+        for (int kp = 0; kp < 4; ++kp) {
+          const int it = hi * 8 + part * 4 + kp, st = it % kExRing;
           if (!(ok = wait_one(W_FULL(st), (it / kExRing) & 1, wc, kSiteKvFull))) break;
           tc_fence_after();
           const uint32_t sb = ring + st * kExStage;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = smem_desc(c_base + k * 2 * kXBox + kk * 32, 16, 1024, kSwizzle128B);
+          for (int kk = 0; kk < 8; ++kk) {  // latent dims 128 kp + 16 kk
+            const uint64_t a = smem_desc(c_base + (2 * kp + (kk >> 2)) * 2 * kXBox + (kk & 3) * 32, 16, 1024, kSwizzle128B);
             if (part == 0)
-              mma_bf16_ss(d, a, smem_desc(sb + kk * 32, 16, 1024, kSwizzle128B), idesc_k, (k | kk) ? 1u : 0u);
+              mma_bf16_ss(d, a, smem_desc(sb + (kk >> 2) * 2 * kXBox + (kk & 3) * 32, 16, 1024, kSwizzle128B), idesc_k,
+                          (kp | kk) ? 1u : 0u);
             else
-              mma_bf16_ss(d, a, smem_desc(sb + kk * 2048, kXBox, 1024, kSwizzle128B), idesc_v, (k | kk) ? 1u : 0u);
+              mma_bf16_ss(d, a, smem_desc(sb + kk * 2048, 2 * kXBox, 1024, kSwizzle128B), idesc_v, (kp | kk) ? 1u : 0u);
           }
           mma_commit(W_EMPTY(st));
         }
@@ -155,7 +166,7 @@ __global__ void __launch_bounds__(kXThreads, 1) mla_expand_kernel(const __grid_c
       const int buf = hi & 1, h = h0 + hi;
       if (!wait_warp(A_FULL(buf), (hi >> 1) & 1, wc, kSiteDrain)) break;
       tc_fence_after();
-      const int64_t row = ((int64_t)(b * args.H + h) * args.C + rel0 + r) * kXDim;
+      const int64_t row = ((int64_t)(b * args.H + h) * args.C + rel0 + r) * args.ld;
 #pragma unroll 1
       for (int part = 0; part < 2; ++part) {
         __nv_bfloat16* dst = (part ? args.v : args.kn) + row;
@@ -194,7 +205,7 @@ __global__ void __launch_bounds__(kXThreads, 1) mla_expand_kernel(const __grid_c
 
 // ---------------------------------------------------------------- attention over one chunk
 constexpr int kAtRing = 4;                               // 64-key tiles in flight
-constexpr uint32_t kAtKn = 0, kAtKr = 2 * kXBox, kAtV = 3 * kXBox;  // offsets inside a stage
+constexpr uint32_t kAtKn = 0, kAtV = 2 * kXBox, kAtKr = 4 * kXBox;  // offsets inside a stage
 constexpr uint32_t kAtStage = 5 * kXBox;                 // K^N 16 KB, k^R 8 KB, V 16 KB
 constexpr uint32_t kAtP = 2 * kXBox;                     // P: [128 rows][64 keys] bf16, 16 KB
 constexpr uint32_t kAtSmem = 1024 + kAtRing * kAtStage + 2 * kAtP + 256;
@@ -203,8 +214,8 @@ constexpr uint32_t kTxO = 0, kTxS = 128, kTxQ = 256;
 
 struct AttendArgs {
   CUtensorMap map_kvc;  // cache rows (k^R at x = 512): bf16 {576, num_pages * 64}, box {64, 64}, 128-byte swizzle
-  CUtensorMap map_kn;   // K^N workspace: bf16 {128, C, B * H}, box {64, 64, 1}, 128-byte swizzle
-  CUtensorMap map_v;    // V workspace: the same shape and box
+  CUtensorMap map_kv;   // workspace rows [K^N | V] as bf16 {64, C, 4 blocks (128 B apart), B * H},
+                        // box {64, 64, 4, 1}: a tile's keys and values in one copy, 128-byte swizzle
   const __nv_bfloat16* q_nope;  // [B][s_q][H][128]
   const __nv_bfloat16* q_rope;  // [B][s_q][H][64]
   const int32_t* block_table;
@@ -249,8 +260,7 @@ __global__ void __launch_bounds__(kXThreads, 1) mla_attend_kernel(const __grid_c
     }
     *abort_flag = 0;
     prefetch_tensormap(&args.map_kvc);
-    prefetch_tensormap(&args.map_kn);
-    prefetch_tensormap(&args.map_v);
+    prefetch_tensormap(&args.map_kv);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -284,11 +294,8 @@ __global__ void __launch_bounds__(kXThreads, 1) mla_attend_kernel(const __grid_c
       if (i >= kAtRing && !wait_one(KV_EMPTY(st), ((i / kAtRing) - 1) & 1, wc, kSiteKvEmpty)) break;
       const uint32_t sb = base + st * kAtStage;
       mbar_arrive_expect_tx(KV_FULL(st), kAtStage);
-      tma_load_3d(sb + kAtKn, &args.map_kn, KV_FULL(st), 0, rel, (int)bh, pol);
-      tma_load_3d(sb + kAtKn + kXBox, &args.map_kn, KV_FULL(st), 64, rel, (int)bh, pol);
+      tma_load_4d(sb + kAtKn, &args.map_kv, KV_FULL(st), 0, rel, 0, (int)bh, pol);  // K^N, then V
       tma_load_2d(sb + kAtKr, &args.map_kvc, KV_FULL(st), 512, bt[key0 / 64] * 64, pol);
-      tma_load_3d(sb + kAtV, &args.map_v, KV_FULL(st), 0, rel, (int)bh, pol);
-      tma_load_3d(sb + kAtV + kXBox, &args.map_v, KV_FULL(st), 64, rel, (int)bh, pol);
     }
   } else if (warp == 1 && lane == 0 && n > 0) {
     const uint32_t idesc_s = idesc_bf16_f32(128, 64, 0, 0), idesc_o = idesc_bf16_f32(128, 128, 0, 1);

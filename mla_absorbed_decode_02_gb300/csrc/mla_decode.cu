@@ -319,9 +319,10 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 int32_t encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, const uint64_t* dims,
                    const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle sw) {
-  cuuint64_t gd[3];
-  cuuint64_t gs[2];
-  cuuint32_t bx[3], es[3] = {1, 1, 1};
+  cuuint64_t gd[5];
+  cuuint64_t gs[4];
+  cuuint32_t bx[5], es[5] = {1, 1, 1, 1, 1};
+  if (rank < 1 || rank > 5) return MLA_ERR_INVALID_ARG;
   for (int i = 0; i < rank; ++i) {
     gd[i] = dims[i];
     bx[i] = box[i];
@@ -715,7 +716,7 @@ struct ExtendLayout {
 };
 static ExtendLayout extend_layout(const mla_extend_params* p) {
   ExtendLayout l;
-  l.kv = align256((size_t)p->batch * p->num_heads * p->chunk_tokens * kXDim * 2);
+  l.kv = align256((size_t)p->batch * p->num_heads * p->chunk_tokens * kXDim * 2);  // half of the [K^N | V] rows
   l.acc_o = align256((size_t)p->batch * p->s_q * p->num_heads * kXDim * 4);
   l.acc_lse = align256((size_t)p->batch * p->s_q * p->num_heads * 4);
   l.total = 2 * l.kv + l.acc_o + l.acc_lse;
@@ -752,11 +753,12 @@ static int32_t cache_map(CUtensorMap* m, const void* kv_pages, int32_t num_pages
   return encode_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_pages, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// The workspace's [K^N | V] rows (256 values) as {64, C rows, 4 blocks of 64, B * H}.
 static int32_t workspace_map(CUtensorMap* m, const void* buf, const mla_extend_params* p) {
-  const uint64_t d[3] = {(uint64_t)kXDim, (uint64_t)p->chunk_tokens, (uint64_t)p->batch * p->num_heads};
-  const uint64_t s[2] = {(uint64_t)kXDim * 2, (uint64_t)p->chunk_tokens * kXDim * 2};
-  const uint32_t bx[3] = {64, 64, 1};
-  return encode_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, buf, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B);
+  const uint64_t d[4] = {64, (uint64_t)p->chunk_tokens, 4, (uint64_t)p->batch * p->num_heads};
+  const uint64_t s[3] = {2 * kXDim * 2, 128, (uint64_t)p->chunk_tokens * 2 * kXDim * 2};
+  const uint32_t bx[4] = {64, 64, 4, 1};
+  return encode_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, buf, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Maps and grid of the expansion; the caller sets chunk_start and launches.
@@ -766,18 +768,18 @@ static int32_t expand_setup(const mla_extend_params* p, const void* kv_pages, co
   std::memset(a, 0, sizeof *a);
   int32_t st;
   if ((st = cache_map(&a->map_kvc, kv_pages, p->num_pages))) return st;
-  {
-    const uint64_t d[3] = {512, (uint64_t)kXDim, (uint64_t)p->num_heads};
-    const uint64_t s[2] = {512 * 2, (uint64_t)kXDim * 512 * 2};
-    const uint32_t bx[3] = {64, 128, 1};
-    if ((st = encode_map(&a->map_wuk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w_uk, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B)))
+  {  // W_UK [H][128 n][512 k] as {64 k, 128 n, 8 k-chunks, H}: two chunks per box
+    const uint64_t d[4] = {64, (uint64_t)kXDim, 8, (uint64_t)p->num_heads};
+    const uint64_t s[3] = {512 * 2, 128, (uint64_t)kXDim * 512 * 2};
+    const uint32_t bx[4] = {64, 128, 2, 1};
+    if ((st = encode_map(&a->map_wuk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, w_uk, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B)))
       return st;
   }
-  {
-    const uint64_t d[3] = {(uint64_t)kXDim, 512, (uint64_t)p->num_heads};
-    const uint64_t s[2] = {(uint64_t)kXDim * 2, (uint64_t)512 * kXDim * 2};
-    const uint32_t bx[3] = {64, 64, 1};
-    if ((st = encode_map(&a->map_wuv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w_uv, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B)))
+  {  // W_UV [H][512 k][128 n] as {64 n, 512 k, 2 n-blocks, H}: 128 k rows of both blocks per box
+    const uint64_t d[4] = {64, 512, 2, (uint64_t)p->num_heads};
+    const uint64_t s[3] = {(uint64_t)kXDim * 2, 128, (uint64_t)512 * kXDim * 2};
+    const uint32_t bx[4] = {64, 128, 2, 1};
+    if ((st = encode_map(&a->map_wuv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, w_uv, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B)))
       return st;
   }
   a->block_table = block_table;
@@ -789,6 +791,7 @@ static int32_t expand_setup(const mla_extend_params* p, const void* kv_pages, co
   a->C = p->chunk_tokens;
   a->s_q = p->s_q;
   a->max_pages_per_seq = p->max_pages_per_seq;
+  a->ld = kXDim;  // separate K^N and V buffers (the extend's workspace interleaves them)
   a->timeout_ns = (uint64_t)(p->timeout_us ? p->timeout_us : 2000000) * 1000ull;
   // heads per CTA: as many as keep at least two CTAs per SM busy (the latent tile is loaded once
   // per CTA and reused for all of its heads)
@@ -857,8 +860,8 @@ int32_t mla_extend(const mla_extend_params* p, const void* q_nope, const void* q
   if ((st = extend_attrs(&dinfo))) return st;
   const ExtendLayout lay = extend_layout(p);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* kn = ws;
-  void* vv = ws + lay.kv;
+  void* kn = ws;                                      // rows [K^N | V] of 256 values
+  void* vv = ws + kXDim * 2;
   float* acc_o = reinterpret_cast<float*>(ws + 2 * lay.kv);
   float* acc_lse = reinterpret_cast<float*>(ws + 2 * lay.kv + lay.acc_o);
   ExpandArgs ea;
@@ -868,7 +871,8 @@ int32_t mla_extend(const mla_extend_params* p, const void* q_nope, const void* q
   AttendArgs aa;
   std::memset(&aa, 0, sizeof aa);
   aa.map_kvc = ea.map_kvc;
-  if ((st = workspace_map(&aa.map_kn, kn, p)) || (st = workspace_map(&aa.map_v, vv, p))) return st;
+  ea.ld = 2 * kXDim;
+  if ((st = workspace_map(&aa.map_kv, kn, p))) return st;
   aa.q_nope = static_cast<const __nv_bfloat16*>(q_nope);
   aa.q_rope = static_cast<const __nv_bfloat16*>(q_rope);
   aa.block_table = block_table;
