@@ -19,17 +19,9 @@
 // d_nope = d_v = 128 (DeepSeek-V3's per-head dims), d_c = 512, d_r = 64, pages of 64 rows.
 #pragma once
 #include "common.cuh"
+#include "tma4d.cuh"
 
 namespace mla {
-
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z,
-                                            int w, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
-      "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy)
-      : "memory");
-}
 
 constexpr int kXThreads = 192;                    // warp 0: TMA, warp 1: MMA, warps 2..5: row work
 constexpr int kXDim = 128;                        // d_nope = d_v

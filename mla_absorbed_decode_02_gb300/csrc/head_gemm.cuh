@@ -7,6 +7,7 @@
 // columns, K in chunks of 64 staged by TMA.
 #pragma once
 #include "common.cuh"
+#include "tma4d.cuh"
 
 namespace mla {
 
@@ -24,7 +25,7 @@ __host__ __device__ constexpr uint32_t hg_stage_bytes(int n_tile) { return kHgAB
 
 struct HeadGemmArgs {
   CUtensorMap map_a;  // A: bf16 {K, H, T}, box {64, 1, 128}, 128-byte swizzle
-  CUtensorMap map_w;  // W: bf16 {N, K, H}, box {64, 64, 1}, 128-byte swizzle
+  CUtensorMap map_w;  // W: bf16 {64, K, N / 64 blocks (128 B apart), H}, box {64, 64, n_tile / 64, 1}, 128-byte swizzle
   void* c;            // C: bf16 [T][H][N]
   int32_t T, H, K, N, n_tile, stages;  // stages: K chunks in flight (2..6)
   uint64_t timeout_ns;
@@ -74,8 +75,9 @@ __global__ void __launch_bounds__(kHgThreads, 1) mla_head_gemm_kernel(const __gr
       const uint32_t st = k % S, sbase = base + st * stage_bytes;
       mbar_arrive_expect_tx(bars + 8 * st, kHgABytes + nblk * kHgBBlock);
       tma_load_3d(sbase, &args.map_a, bars + 8 * st, k * kHgKChunk, h, t0, pol);
-      for (int j = 0; j < nblk; ++j)
-        tma_load_3d(sbase + kHgABytes + j * kHgBBlock, &args.map_w, bars + 8 * st, n0 + 64 * j, k * kHgKChunk, h, pol);
+      // the stage's n_tile / 64 blocks of W in one copy (a copy costs the issuing thread the same
+      // whatever its size)
+      tma_load_4d(sbase + kHgABytes, &args.map_w, bars + 8 * st, 0, k * kHgKChunk, n0 / 64, h, pol);
     };
     bool ok = true;
     for (int k = 0; k < nk && k < S; ++k) load(k);

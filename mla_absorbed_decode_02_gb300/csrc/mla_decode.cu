@@ -648,11 +648,12 @@ static int32_t launch_head_gemm(int32_t T, int32_t H, int32_t K, int32_t N, cons
     if ((st = encode_map(&g.map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B)))
       return st;
   }
-  {
-    const uint64_t d[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)H};
-    const uint64_t s[2] = {(uint64_t)N * 2, (uint64_t)K * N * 2};
-    const uint32_t bx[3] = {64, (uint32_t)kHgKChunk, 1};
-    if ((st = encode_map(&g.map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B)))
+  g.n_tile = N % kHgMaxN == 0 ? kHgMaxN : (N % 128 == 0 ? 128 : 64);
+  {  // W [H][K][N] as {64, K rows, N / 64 blocks (128 B apart), H}: a stage's blocks in one box
+    const uint64_t d[4] = {64, (uint64_t)K, (uint64_t)(N / 64), (uint64_t)H};
+    const uint64_t s[3] = {(uint64_t)N * 2, 128, (uint64_t)K * N * 2};
+    const uint32_t bx[4] = {64, (uint32_t)kHgKChunk, (uint32_t)(g.n_tile / 64), 1};
+    if ((st = encode_map(&g.map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, w, d, s, bx, CU_TENSOR_MAP_SWIZZLE_128B)))
       return st;
   }
   g.c = c;
@@ -660,7 +661,6 @@ static int32_t launch_head_gemm(int32_t T, int32_t H, int32_t K, int32_t N, cons
   g.H = H;
   g.K = K;
   g.N = N;
-  g.n_tile = N % kHgMaxN == 0 ? kHgMaxN : (N % 128 == 0 ? 128 : 64);
   g.timeout_ns = 2000000000ull;
   // K chunks in flight: all of them (up to six, 192 KB) when the grid fits one CTA per SM, two
   // (two CTAs per SM) when it is larger
