@@ -89,9 +89,17 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def roofline_time_s(flops: int, nbytes: int, peaks) -> tuple[float, str]:
+def qk8_tensor_peak(peaks) -> float:
+    """Tensor peak (TFLOP/s) of the FP8-QK decode's mix of MMAs: the latent part of QK (d_c of the
+    d_c + d_r QK dims of every pair) on E4M3 codes at twice the measured bf16 rate (the nominal
+    fp8 : bf16 ratio of the tensor cores), the RoPE part of QK and all of PV at the bf16 rate."""
+    fp8, bf16 = 2 * D_C, 2 * D_R + 2 * D_C  # FLOPs per head and pair
+    return peaks["bf16_tflops"] * (fp8 + bf16) / (fp8 / 2 + bf16)
+
+
+def roofline_time_s(flops: int, nbytes: int, peaks, qk8: bool = False) -> tuple[float, str]:
     t_b = nbytes / (peaks["hbm_gbs"] * 1e9)
-    t_f = flops / (peaks["bf16_tflops"] * 1e12)
+    t_f = flops / ((qk8_tensor_peak(peaks) if qk8 else peaks["bf16_tflops"]) * 1e12)
     return (t_b, "hbm") if t_b >= t_f else (t_f, "tensor")
 
 
@@ -272,58 +280,71 @@ def _device_inputs(w, dev):
     return host, {k: v.to(dev) for k, v in host.items()}
 
 
-def _params(w, token_group=0):
+def _params(w, token_group=0, qk_fp8=False):
     from mla_absorbed_decode_02_gb300 import (MlaDecodeParams, MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_OUT_BF16,
                                               MLA_OUT_F32)
     return MlaDecodeParams.make(w.batch, w.s_q, w.num_heads, w.num_pages, w.block_table.shape[1], causal=w.causal,
                                 kv_dtype=MLA_KV_FP8_E4M3 if w.kv_dtype == "fp8" else MLA_KV_BF16,
                                 out_dtype=MLA_OUT_F32 if w.out_dtype == "f32" else MLA_OUT_BF16,
-                                token_group=token_group)
+                                token_group=token_group, qk_fp8=int(qk_fp8))
 
 
-def _accounting(w, peaks):
+def _accounting(w, peaks, qk8=False):
     flops = algorithmic_flops(w.seqlens, w.s_q, w.num_heads, w.causal)
     row_bytes = 656 if w.kv_dtype == "fp8" else 1152
     nbytes = algorithmic_bytes(w.seqlens, w.s_q, w.num_heads, row_bytes, 4 if w.out_dtype == "f32" else 2)
-    t_roof, bound = roofline_time_s(flops, nbytes, peaks)
+    t_roof, bound = roofline_time_s(flops, nbytes, peaks, qk8)
     return flops, nbytes, row_bytes, t_roof, bound
 
 
-def _roofline(w, name, peaks, t_dec):
+def _roofline(w, name, peaks, t_dec, qk8=False):
     """Roofline object of the decode kernel: algorithmic bytes (or FLOPs) per launch over its event time."""
-    flops, nbytes, _, _, bound = _accounting(w, peaks)
+    flops, nbytes, _, _, bound = _accounting(w, peaks, qk8)
     if bound == "hbm":
         achieved = nbytes / t_dec / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} (copy, burst)"}
+    elif qk8:
+        achieved, peak = flops / t_dec / 1e12, qk8_tensor_peak(peaks)
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{peaks['source']} (cuBLAS bf16, burst; the QK latent part at 2x that rate)"}
     else:
         achieved = flops / t_dec / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "peak_source": f"{peaks['source']} (cuBLAS bf16, burst)"}
     roof["traffic"] = committed_traffic(name)
-    roof["kernel"] = "mla_decode_fp8_kernel" if w.kv_dtype == "fp8" else "mla_decode_bf16_kernel"
+    roof["kernel"] = ("mla_decode_fp8qk_kernel" if qk8 else
+                      "mla_decode_fp8_kernel" if w.kv_dtype == "fp8" else "mla_decode_bf16_kernel")
     roof["kernel_ms"] = t_dec * 1e3
     return roof
 
 
-def time_workload(w, name, peaks, steps, warmup, dev, flush, dist=None, token_group=0):
+def time_workload(w, name, peaks, steps, warmup, dev, flush, dist=None, token_group=0, qk_fp8=False):
     """Device timing of one workload, inputs resident in HBM, L2 flushed before every step.
 
     Pass 1 times whole steps (decode kernel + LSE combine, nothing between the two launches, so
     the combine starts as a programmatic dependent of the decode kernel); pass 2 times the decode
     kernel alone (an event right after it).  Both report the median over `steps` steps after
-    `warmup` untimed ones."""
+    `warmup` untimed ones.  qk_fp8: the FP8-QK decode, its query quantised on the device first
+    (mla_quantize_q_fp8, counted in both passes)."""
     import torch
     from mla_absorbed_decode_02_gb300 import (Decoder, mla_combine, mla_decode_splitkv, mla_device_error,
-                                              mla_get_scheduler_metadata)
+                                              mla_get_scheduler_metadata, mla_quantize_q_fp8)
     host, d = _device_inputs(w, dev)
-    p = _params(w, token_group)
+    p = _params(w, token_group, qk_fp8)
     dec = Decoder(p, dev)
     out, lse = dec.new_outputs()
     stream = torch.cuda.current_stream(dev)
     mla_get_scheduler_metadata(p, d["seq"], dec.sched, stream)
+    rows = w.batch * w.s_q * w.num_heads
+    q8 = torch.empty((rows, 656), dtype=torch.uint8, device=dev) if qk_fp8 else None
 
     def decode():
+        if qk_fp8:
+            mla_quantize_q_fp8(d["q_nope"], d["q_rope"], q8, rows, stream)
+            mla_decode_splitkv(p, q8, None, d["kv"], d["bt"], d["seq"], w.scale, out, lse, dec.sched, dec.workspace,
+                               stream)
+            return
         mla_decode_splitkv(p, d["q_nope"], d["q_rope"], d["kv"], d["bt"], d["seq"], w.scale, out, lse, dec.sched,
                            dec.workspace, stream)
 
@@ -566,20 +587,22 @@ def run_ours(args, w, peaks, world, rank, local):
         clocks = ClockSampler(local)
         clocks.start()
         time.sleep(0.3)
-        # (fp8_mtp2 twice: one CTA pair per new token, and both new tokens of a sequence on shared
-        # pages, token group 2, which reads the cache once)
-        for name, grp in (("uniform4k", 0), ("long", 0), ("fp8_mtp2", 0), ("fp8_mtp2", 2)):
-            if name == args.workload and grp == args.token_group:
+        # (fp8_mtp2 three times: one CTA pair per new token; both new tokens of a sequence on shared
+        # pages, token group 2, which reads the cache once; and the opt-in FP8-QK decode)
+        for name, grp, qk8 in (("uniform4k", 0, False), ("long", 0, False), ("fp8_mtp2", 0, False),
+                               ("fp8_mtp2", 2, False), ("fp8_mtp2", 0, True)):
+            if name == args.workload and grp == args.token_group and not qk8:
                 continue
             wk = mw.make_workload(WORKLOAD_INDEX[name])
-            rk = time_workload(wk, name, peaks, args.steps, args.warmup, dev, flush, token_group=grp)
-            _, _, _, tr, _ = _accounting(wk, peaks)
-            per[name + (f"_token_group{grp}" if grp else "")] = {
+            rk = time_workload(wk, name, peaks, args.steps, args.warmup, dev, flush, token_group=grp, qk_fp8=qk8)
+            _, _, _, tr, _ = _accounting(wk, peaks, qk8)
+            key = name + (f"_token_group{grp}" if grp else "") + ("_qk_fp8" if qk8 else "")
+            per[key] = {
                 "value": 100.0 * tr / rk["t_step"], "ms_per_step": rk["t_step"] * 1e3,
                 "kernel_ms": rk["t_dec"] * 1e3,
-                "roofline": _roofline(wk, name + (f"_token_group{grp}" if grp else ""), peaks, rk["t_dec"]),
+                "roofline": _roofline(wk, key, peaks, rk["t_dec"], qk8),
                 "config": {"batch": wk.batch, "s_q": wk.s_q, "kv_dtype": wk.kv_dtype, "units": rk["dec"].num_units,
-                           "token_group": grp or 1,
+                           "token_group": grp or 1, "qk": "e4m3 codes (tcgen05 kind::f8f6f4)" if qk8 else "bf16",
                            "seqlens": f"{int(wk.seqlens.min())}..{int(wk.seqlens.max())} "
                                       f"(sum {int(wk.seqlens.sum())})"}}
             del rk, wk

@@ -91,7 +91,15 @@ typedef struct mla_decode_params {
                                 cluster of 2G CTAs, pages multicast to every pair); 1..4 and dividing
                                 s_q; 0 = 1.  Clusters of 4 / 8 CTAs occupy 144 / 120 of GB300's 152 SMs,
                                 so G > 1 pays where DRAM, not the SMs, bounds the decode */
-  int32_t reserved[4];       /* must be zero */
+  int32_t qk_fp8;            /* FP8 cache only, opt-in: nonzero => QK runs on E4M3 codes on the FP8 tensor
+                                cores ("MLA inference: two computation paths and FlashMLA", exercise 2
+                                "An FP8 KV cache").  The query is then passed quantised like the cache:
+                                q_nope_absorbed points to [B][s_q][H][656 bytes] rows written by
+                                mla_quantize_q_fp8 (the absorbed query's 512 codes, 4 tile scales, q^R
+                                as 64 bf16) and q_rope is not read (may be NULL).  The result is that of
+                                attention with the dequantised query (code x scale), not the bf16 one.
+                                Needs token_group <= 1; 0 = QK on the bf16-expanded cache */
+  int32_t reserved[3];       /* must be zero */
 } mla_decode_params;
 
 /*
@@ -116,8 +124,9 @@ int32_t mla_get_scheduler_metadata(const mla_decode_params* p, const int32_t* ca
 
 /*
  * The decode.
- *   q_nope_absorbed  device bf16 [B][s_q][H][512]  absorbed query q~
- *   q_rope           device bf16 [B][s_q][H][64]   RoPE query q^R
+ *   q_nope_absorbed  device bf16 [B][s_q][H][512]  absorbed query q~ (qk_fp8: the 656-byte rows of
+ *                    mla_quantize_q_fp8)
+ *   q_rope           device bf16 [B][s_q][H][64]   RoPE query q^R (qk_fp8: not read)
  *   kv_pages         device [num_pages][64][576] bf16, or [num_pages][64][656 bytes] FP8 rows
  *   block_table      device int32 [B][max_pages_per_seq]: physical page of logical page i of
  *                    sequence b; entries past ceil(L_b/64) are never read.  Every entry read
@@ -192,6 +201,18 @@ int32_t mla_resolve_num_units(const mla_decode_params* p, int32_t* num_units);
  * launches nothing.  Both buffers 16-byte aligned; asynchronous on stream.
  */
 int32_t mla_quantize_kv_fp8(const void* kv_bf16, void* kv_fp8, int64_t num_tokens, void* stream);
+
+/*
+ * The query of an FP8-QK decode (mla_decode_params.qk_fp8), quantised like a cache row:
+ *   q_nope_absorbed  device bf16 [num_rows][512]  absorbed query q~ (num_rows = B * s_q * H)
+ *   q_rope           device bf16 [num_rows][64]   RoPE query q^R
+ *   q_fp8            device [num_rows][656 bytes]: 512 E4M3 codes of q~, 4 float32 tile scales,
+ *                    then q^R copied unchanged as 64 bf16
+ * Per 128-element tile: the rule of mla_quantize_kv_fp8.  num_rows = 0 launches nothing.  All
+ * buffers 16-byte aligned; asynchronous on stream.
+ */
+int32_t mla_quantize_q_fp8(const void* q_nope_absorbed, const void* q_rope, void* q_fp8, int64_t num_rows,
+                           void* stream);
 
 /*
  * Query absorption ("MLA inference: two computation paths and FlashMLA", section "Two

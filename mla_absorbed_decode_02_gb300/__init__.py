@@ -11,5 +11,5 @@ from ._lib import (  # noqa: F401
     Decoder, MlaDecodeParams, MlaError, library_path, load_library, mla_absorb_query, mla_combine, mla_decode,
     mla_decode_noalloc, mla_project_output, MlaExtendParams, mla_expand_kv, mla_extend, mla_extend_workspace_size,
     mla_decode_splitkv, mla_device_error, mla_get_scheduler_metadata, mla_get_workspace_size, mla_plan_host,
-    mla_quantize_kv_fp8, mla_resolve_num_units, mla_status_string, mla_wait_selftest,
+    mla_quantize_kv_fp8, mla_quantize_q_fp8, mla_resolve_num_units, mla_status_string, mla_wait_selftest,
 )

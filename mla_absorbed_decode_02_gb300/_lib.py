@@ -39,13 +39,13 @@ class MlaDecodeParams(ctypes.Structure):
                 ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("max_pages_per_seq", ctypes.c_int32), ("causal", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("num_units", ctypes.c_int32), ("timeout_us", ctypes.c_int32),
-                ("token_group", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+                ("token_group", ctypes.c_int32), ("qk_fp8", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
     @classmethod
     def make(cls, batch, s_q, num_heads, num_pages, max_pages_per_seq, causal=True, kv_dtype=MLA_KV_BF16,
-             out_dtype=MLA_OUT_BF16, num_units=0, timeout_us=0, page_size=64, token_group=0):
+             out_dtype=MLA_OUT_BF16, num_units=0, timeout_us=0, page_size=64, token_group=0, qk_fp8=0):
         return cls(batch, s_q, num_heads, num_pages, page_size, max_pages_per_seq, int(bool(causal)), kv_dtype,
-                   out_dtype, num_units, timeout_us, token_group)
+                   out_dtype, num_units, timeout_us, token_group, int(qk_fp8))
 
 
 class MlaExtendParams(ctypes.Structure):
@@ -86,6 +86,7 @@ def load_library():
             "mla_wait_selftest": ([i32, vp], i32),
             "mla_decode_noalloc": ([P, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp], i32),
             "mla_quantize_kv_fp8": ([vp, vp, ctypes.c_int64, vp], i32),
+            "mla_quantize_q_fp8": ([vp, vp, vp, ctypes.c_int64, vp], i32),
             "mla_absorb_query": ([i32, i32, i32, vp, vp, vp, vp], i32),
             "mla_project_output": ([i32, i32, i32, vp, vp, vp, vp], i32),
             "mla_extend_workspace_size": ([X, ctypes.POINTER(sz)], i32),
@@ -190,6 +191,12 @@ def mla_quantize_kv_fp8(kv_bf16, kv_fp8, num_tokens: int, stream=None):
     """bf16 cache rows [n, 576] -> 656-byte FP8 rows [n, 656] (codes, tile scales, RoPE)."""
     _check(load_library().mla_quantize_kv_fp8(_ptr(kv_bf16), _ptr(kv_fp8), int(num_tokens), _stream(stream)),
            "mla_quantize_kv_fp8")
+
+
+def mla_quantize_q_fp8(q_nope_absorbed, q_rope, q_fp8, num_rows: int, stream=None):
+    """Query rows for an FP8-QK decode: q~ bf16 [n, 512] and q^R bf16 [n, 64] -> 656-byte rows [n, 656]."""
+    _check(load_library().mla_quantize_q_fp8(_ptr(q_nope_absorbed), _ptr(q_rope), _ptr(q_fp8), int(num_rows),
+                                             _stream(stream)), "mla_quantize_q_fp8")
 
 
 def mla_absorb_query(q_nope, w_uk, q_absorbed, stream=None):

@@ -33,11 +33,11 @@ __device__ __forceinline__ void raise_abort(const WaitCtx& w, int site) {
   if (w.abort_peer) asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(w.abort_peer), "r"(1) : "memory");
 }
 
-// Bounded wait by one thread (the slow path, out of line).  Returns false if
-// the CTA is aborting or the wait ran out (then it raises the abort for this
-// CTA and its peer).
-template <bool kClusterScope = false>
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
+// Bounded wait by one thread (the slow path).  Returns false if the CTA is
+// aborting or the wait ran out (then it raises the abort for this CTA and its
+// peer).
+template <bool kClusterScope>
+__device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
   auto poll = [&]() { return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
@@ -52,17 +52,25 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Wait
   }
 }
 
-// Bounded wait by one thread: one inline poll, then the slow path.
-template <bool kClusterScope = false>
+// The slow path out of line (it keeps the callers' instruction streams short).
+template <bool kClusterScope>
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
+  return wait_poll<kClusterScope>(bar, parity, w, site);
+}
+
+// Bounded wait by one thread: one inline poll, then the slow path -- inline with kInlineSlow
+// (a kernel that re-splits its registers between warpgroups makes no calls: its warps run
+// under different register counts).
+template <bool kClusterScope = false, bool kInlineSlow = false>
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
   if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-  return wait_slow<kClusterScope>(bar, parity, w, site);
+  return kInlineSlow ? wait_poll<kClusterScope>(bar, parity, w, site) : wait_slow<kClusterScope>(bar, parity, w, site);
 }
 
 // Bounded wait by a whole warp; the result is the same in every lane.
-template <bool kClusterScope = false>
+template <bool kClusterScope = false, bool kInlineSlow = false>
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
-  const bool ok = wait_one<kClusterScope>(bar, parity, w, site);
+  const bool ok = wait_one<kClusterScope, kInlineSlow>(bar, parity, w, site);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -75,12 +83,15 @@ __device__ __forceinline__ void drain_delay(uint64_t ns) {
 }
 
 struct DecodeArgs {
-  CUtensorMap map_qr;    // q^R half: bf16 {64, H, NQB}, box {32, 128, 1}, 64-byte swizzle
+  CUtensorMap map_qr;    // q^R half: bf16 {64, H, NQB}, box {32, 128, 1}, 64-byte swizzle (FP8 QK:
+                         // the same view of the RoPE values inside the 656-byte query rows)
   CUtensorMap map_kvc;   // bf16 cache: latent of 64 rows, box {64 dims, 64 rows}, 128-byte swizzle;
-                         // FP8 cache (bytes): the 256 codes of one half, box {256, 64}, no swizzle
+                         // FP8 cache (bytes): the 256 codes of one half, box {256, 64}, no swizzle;
+                         // FP8 QK: one 128-code tile, box {128, 64}, 128-byte swizzle
   CUtensorMap map_kvr;   // RoPE key of 64 rows: bf16 box {32 dims, 64 rows} / bytes {64, 64}, 64-byte swizzle
   CUtensorMap map_kvs;   // FP8 cache: the 4 tile scales of 64 rows, box {16 bytes, 64}, no swizzle
-  const void* q_nope;    // absorbed queries, bf16 [NQB][H][512] (read by threads into tensor memory)
+  const void* q_nope;    // absorbed queries, bf16 [NQB][H][512] (read by threads into tensor memory);
+                         // FP8 QK: 656-byte query rows [NQB][H] (512 codes, 4 scales, RoPE)
   const void* q_rope;    // RoPE queries, bf16 [NQB][H][64] (loaded by TMA; read here only to prefetch into L2)
   const int32_t* block_table;
   const int32_t* seqlens;
@@ -90,7 +101,7 @@ struct DecodeArgs {
   float* o_acc;          // split partials [slots][H][512], normalised
   float* lse_acc;        // [slots][H]
   float scale_log2;      // softmax scale * log2(e)
-  int32_t H, s_q, causal, max_pages, out_f32, num_units, num_qb, kv_fp8;
+  int32_t H, s_q, causal, max_pages, out_f32, num_units, num_qb, kv_fp8, qk_fp8;
   int32_t group;         // G: new tokens per work block; a unit is a cluster of 2G CTAs, one pair per token
   uint64_t timeout_ns;
 };

@@ -160,11 +160,16 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const int32_t* sched, 
 // Serving: Multi-Head Latent Attention at Scale", section "Understanding FP8 Formats:
 // E4M3 vs. E5M2").  One warp per token; lane l owns latent elements [16 l, 16 l + 16),
 // so a tile is 8 lanes.
-__global__ void __launch_bounds__(256) mla_quantize_fp8_kernel(const __nv_bfloat16* kv, uint8_t* out, int64_t n) {
+// (latent row `tok` at lat + tok * lat_stride, its 64 RoPE values at rope + tok * rope_stride: one
+// 576-element cache row, or a query's two arrays)
+__global__ void __launch_bounds__(256) mla_quantize_fp8_kernel(const __nv_bfloat16* lat, int64_t lat_stride,
+                                                               const __nv_bfloat16* rope, int64_t rope_stride,
+                                                               uint8_t* out, int64_t n) {
   const int64_t tok = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (tok >= n) return;
-  const __nv_bfloat16* src = kv + tok * 576;
+  const __nv_bfloat16* src = lat + tok * lat_stride;
+  const __nv_bfloat16* src_r = rope + tok * rope_stride;
   uint8_t* dst = out + tok * 656;
   float x[16];
   {
@@ -192,7 +197,7 @@ __global__ void __launch_bounds__(256) mla_quantize_fp8_kernel(const __nv_bfloat
   }
   *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
   if ((lane & 7) == 0) *reinterpret_cast<float*>(dst + 512 + 4 * (lane >> 3)) = scale;
-  if (lane < 8) *reinterpret_cast<uint4*>(dst + 528 + 16 * lane) = *reinterpret_cast<const uint4*>(src + 512 + 8 * lane);
+  if (lane < 8) *reinterpret_cast<uint4*>(dst + 528 + 16 * lane) = *reinterpret_cast<const uint4*>(src_r + 8 * lane);
 }
 
 // ----------------------------------------------------------------- bounded-wait self test
@@ -226,6 +231,7 @@ struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
   int max_clusters[5] = {0, 0, 0, 0, 0};  // [G]: clusters of 2G decode CTAs that fit at once
+  bool qk8_ok = false;                    // the FP8-QK kernel's register count allows its re-split
 };
 std::mutex g_mu;
 DeviceInfo g_dev[64];
@@ -239,9 +245,16 @@ int32_t device_info(DeviceInfo** out) {
   if (!d.ready) {
     if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
     for (const void* k : {(const void*)mla_decode_bf16_kernel, (const void*)mla_decode_fp8_kernel,
-                          (const void*)mla_decode_bf16_group_kernel, (const void*)mla_decode_fp8_group_kernel})
+                          (const void*)mla_decode_bf16_group_kernel, (const void*)mla_decode_fp8_group_kernel,
+                          (const void*)mla_decode_fp8qk_kernel})
       if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
         return MLA_ERR_CUDA;
+    {  // the FP8-QK kernel re-splits its registers between warpgroups: the launch must hold at least
+       // what the re-split hands out, or a warpgroup's request would wait forever
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, (const void*)mla_decode_fp8qk_kernel) != cudaSuccess) return MLA_ERR_CUDA;
+      d.qk8_ok = fa.numRegs * 2 >= kRegsSoftmax + kRegsOther;
+    }
     for (int G = 1; G <= 4; ++G) {  // GPCs hold whole clusters: bigger ones leave SMs idle
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * G * (d.sm_count / (2 * G)), 1, 1);
@@ -278,14 +291,16 @@ int32_t check_params(const mla_decode_params* p) {
   if (!p) return MLA_ERR_INVALID_ARG;
   if (p->batch < 1 || p->num_heads < 1 || p->num_pages < 1 || p->max_pages_per_seq < 1) return MLA_ERR_INVALID_ARG;
   if (p->s_q < 1 || p->page_size < 1 || p->num_units < 0 || p->timeout_us < 0) return MLA_ERR_INVALID_ARG;
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 3; ++i)
     if (p->reserved[i] != 0) return MLA_ERR_INVALID_ARG;
+  if (p->qk_fp8 != 0 && (p->qk_fp8 != 1 || p->kv_dtype != MLA_KV_FP8_E4M3)) return MLA_ERR_INVALID_ARG;
   if (p->token_group < 0 || p->token_group > 4 || (p->token_group > 0 && p->s_q % p->token_group != 0))
     return MLA_ERR_INVALID_ARG;
   if (p->kv_dtype != MLA_KV_BF16 && p->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
   if (p->out_dtype != MLA_OUT_BF16 && p->out_dtype != MLA_OUT_F32) return MLA_ERR_INVALID_ARG;
   if (p->page_size != 64 || p->s_q > 8 || p->num_heads > 128) return MLA_ERR_UNSUPPORTED;
   if ((int64_t)p->batch * p->s_q > (1 << 24) || (int64_t)p->num_pages * 64 > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  if (p->qk_fp8 && p->token_group > 1) return MLA_ERR_UNSUPPORTED;
   return MLA_OK;
 }
 
@@ -341,10 +356,10 @@ struct MapKey {
   int dev;
   const void* q_rope;
   const void* kv;
-  int H, NQB, num_pages, kv_dtype;
+  int H, NQB, num_pages, kv_dtype, qk8;  // qk8: q_rope is the 656-byte FP8 query rows
   bool operator==(const MapKey& o) const {
     return dev == o.dev && q_rope == o.q_rope && kv == o.kv && H == o.H && NQB == o.NQB &&
-           num_pages == o.num_pages && kv_dtype == o.kv_dtype;
+           num_pages == o.num_pages && kv_dtype == o.kv_dtype && qk8 == o.qk8;
   }
 };
 struct MapSet {
@@ -359,10 +374,13 @@ int g_map_next = 0;
 int32_t encode_maps(const MapKey& k, MapSet* m) {
   int32_t st;
   {
+    // q^R: its own bf16 array, or (FP8 QK) the 64 bf16 at byte 528 of each 656-byte query row
+    const void* q = k.qk8 ? static_cast<const void*>(static_cast<const char*>(k.q_rope) + 528) : k.q_rope;
+    const uint64_t row = k.qk8 ? 656 : 64 * 2;
     const uint64_t d[3] = {64, (uint64_t)k.H, (uint64_t)k.NQB};
-    const uint64_t s[2] = {64 * 2, (uint64_t)k.H * 64 * 2};
+    const uint64_t s[2] = {row, (uint64_t)k.H * row};
     const uint32_t bx[3] = {32, 128, 1};
-    if ((st = encode_map(&m->qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k.q_rope, d, s, bx, CU_TENSOR_MAP_SWIZZLE_64B)))
+    if ((st = encode_map(&m->qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, d, s, bx, CU_TENSOR_MAP_SWIZZLE_64B)))
       return st;
   }
   if (k.kv_dtype == MLA_KV_BF16) {
@@ -377,9 +395,13 @@ int32_t encode_maps(const MapKey& k, MapSet* m) {
   } else {  // FP8 rows of 656 bytes: 512 codes, 4 float32 scales, 64 bf16 RoPE
     const uint64_t d[2] = {656, (uint64_t)k.num_pages * 64};
     const uint64_t s[1] = {656};
-    const uint32_t bc[2] = {256, 64}, br[2] = {64, 64}, bs[2] = {16, 64};
-    if ((st = encode_map(&m->kvc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k.kv, d, s, bc, CU_TENSOR_MAP_SWIZZLE_NONE)))
+    const uint32_t bc[2] = {256, 64}, bc8[2] = {128, 64}, br[2] = {64, 64}, bs[2] = {16, 64};
+    if (k.qk8) {  // one 128-code tile in the swizzled K-major layout the QK MMAs read
+      if ((st = encode_map(&m->kvc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k.kv, d, s, bc8, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return st;
+    } else if ((st = encode_map(&m->kvc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k.kv, d, s, bc, CU_TENSOR_MAP_SWIZZLE_NONE))) {
       return st;
+    }
     if ((st = encode_map(&m->kvr, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k.kv, d, s, br, CU_TENSOR_MAP_SWIZZLE_64B)))
       return st;
     if ((st = encode_map(&m->kvs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k.kv, d, s, bs, CU_TENSOR_MAP_SWIZZLE_NONE)))
@@ -480,12 +502,16 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
                            void* out, float* lse, const void* sched, void* workspace, void* stream) {
   int32_t st = check_params(p);
   if (st != MLA_OK) return st;
-  const void* ptrs[] = {q_nope_absorbed, q_rope, kv_pages, block_table, cache_seqlens, out, lse, sched, workspace};
+  // (FP8 QK: the query is the FP8 rows alone; q_rope is not read)
+  const bool qk8 = p->qk_fp8 != 0;
+  const void* ptrs[] = {q_nope_absorbed, qk8 ? q_nope_absorbed : q_rope, kv_pages, block_table, cache_seqlens,
+                        out, lse, sched, workspace};
   for (const void* q : ptrs)
     if (!q || !aligned16(q)) return MLA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return MLA_ERR_INVALID_ARG;  // the kernel takes row maxima before scaling
   DeviceInfo* dinfo = nullptr;
   if ((st = device_info(&dinfo)) != MLA_OK) return st;
+  if (qk8 && !dinfo->qk8_ok) return MLA_ERR_CUDA;
   int32_t U = 0;
   if ((st = resolve_units(p, &U)) != MLA_OK) return st;
   const int H = p->num_heads, NQB = p->batch * p->s_q, G = resolve_group(p);
@@ -496,10 +522,11 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
   {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
-    const MapKey key{dev, q_rope, kv_pages, H, NQB, p->num_pages, p->kv_dtype};
+    const MapKey key{dev, qk8 ? q_nope_absorbed : q_rope, kv_pages, H, NQB, p->num_pages, p->kv_dtype, qk8 ? 1 : 0};
     if ((st = tensor_maps(key, &a)) != MLA_OK) return st;
   }
   a.kv_fp8 = p->kv_dtype == MLA_KV_FP8_E4M3;
+  a.qk_fp8 = qk8 ? 1 : 0;
   a.q_nope = q_nope_absorbed;
   a.q_rope = q_rope;
   a.block_table = block_table;
@@ -522,7 +549,7 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * G * U, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(qk8 ? kThreadsQk8 : kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = static_cast<cudaStream_t>(stream);
   // one unit = a cluster of 2G CTAs; programmatic dependent launch: the kernel's set-up
@@ -537,10 +564,11 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = G > 1 ? (a.kv_fp8 ? cudaLaunchKernelEx(&cfg, mla_decode_fp8_group_kernel, a)
-                                          : cudaLaunchKernelEx(&cfg, mla_decode_bf16_group_kernel, a))
-                               : (a.kv_fp8 ? cudaLaunchKernelEx(&cfg, mla_decode_fp8_kernel, a)
-                                           : cudaLaunchKernelEx(&cfg, mla_decode_bf16_kernel, a));
+  const cudaError_t e = qk8      ? cudaLaunchKernelEx(&cfg, mla_decode_fp8qk_kernel, a)
+                        : G > 1 ? (a.kv_fp8 ? cudaLaunchKernelEx(&cfg, mla_decode_fp8_group_kernel, a)
+                                            : cudaLaunchKernelEx(&cfg, mla_decode_bf16_group_kernel, a))
+                                : (a.kv_fp8 ? cudaLaunchKernelEx(&cfg, mla_decode_fp8_kernel, a)
+                                            : cudaLaunchKernelEx(&cfg, mla_decode_bf16_kernel, a));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -615,8 +643,22 @@ int32_t mla_quantize_kv_fp8(const void* kv_bf16, void* kv_fp8, int64_t num_token
   if (num_tokens == 0) return MLA_OK;
   const int64_t blocks = (num_tokens + 7) / 8;
   if (blocks > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  const __nv_bfloat16* kv = static_cast<const __nv_bfloat16*>(kv_bf16);
   mla_quantize_fp8_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const __nv_bfloat16*>(kv_bf16), static_cast<uint8_t*>(kv_fp8), num_tokens);
+      kv, 576, kv + 512, 576, static_cast<uint8_t*>(kv_fp8), num_tokens);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int32_t mla_quantize_q_fp8(const void* q_nope_absorbed, const void* q_rope, void* q_fp8, int64_t num_rows,
+                           void* stream) {
+  if (!q_nope_absorbed || !q_rope || !q_fp8 || num_rows < 0) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope_absorbed) || !aligned16(q_rope) || !aligned16(q_fp8)) return MLA_ERR_INVALID_ARG;
+  if (num_rows == 0) return MLA_OK;
+  const int64_t blocks = (num_rows + 7) / 8;
+  if (blocks > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  mla_quantize_fp8_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(q_nope_absorbed), 512, static_cast<const __nv_bfloat16*>(q_rope), 64,
+      static_cast<uint8_t*>(q_fp8), num_rows);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

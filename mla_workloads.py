@@ -91,6 +91,14 @@ def quantize_fp8_rows(c: np.ndarray, kr_bits: np.ndarray) -> np.ndarray:
     return rows
 
 
+def quantize_query_fp8(w) -> np.ndarray:
+    """The workload's query in the FP8 row layout (as a cache row: absorbed query -> 512 codes and 4
+    tile scales, RoPE query copied): uint8 [B, s_q, H, 656], the input of an FP8-QK decode."""
+    lat = (w.q_nope.astype(np.uint32) << 16).view(np.float32).reshape(-1, D_C)
+    rows = quantize_fp8_rows(lat, w.q_rope.reshape(-1, D_R))
+    return rows.reshape(w.batch, w.s_q, w.num_heads, FP8_ROW_BYTES)
+
+
 def _fill_pool(rng: np.random.Generator, num_pages: int, kv_dtype: str) -> np.ndarray:
     """N(0,1) page pool, generated in chunks of pages to bound host memory."""
     if kv_dtype == "bf16":

@@ -87,6 +87,23 @@ def e4m3_to_f64(code: int) -> float:
     return _load().orc_e4m3_to_f64(int(code) & 0xFF)
 
 
+def fp8_rows_to_f64(rows: np.ndarray, d_c: int = 512, d_r: int = 64):
+    """Rows in the FP8 cache-row layout ("MLA and FP8 MoE Serving: Multi-Head Latent Attention at
+    Scale", section "Understanding FP8 Formats: E4M3 vs. E5M2"): d_c E4M3 codes, one float32 scale per
+    128 codes, d_r bf16 values -> (latent float64 [..., d_c] = code x scale, exact; RoPE float64
+    [..., d_r]).  The same decoding the C oracle applies to an FP8 cache, for rows held elsewhere
+    (the quantised query of an FP8-QK decode)."""
+    rows = np.ascontiguousarray(rows, dtype=np.uint8)
+    lead = rows.shape[:-1]
+    assert rows.shape[-1] == d_c + 4 * (d_c // 128) + 2 * d_r
+    r = rows.reshape(-1, rows.shape[-1])
+    table = np.array([e4m3_to_f64(c) for c in range(256)], np.float64)
+    scales = np.ascontiguousarray(r[:, d_c:d_c + 4 * (d_c // 128)]).view(np.float32).astype(np.float64)
+    lat = table[r[:, :d_c]] * np.repeat(scales, 128, axis=1)
+    rope = bf16_bits_to_f64(np.ascontiguousarray(r[:, d_c + 4 * (d_c // 128):]).view(np.uint16))
+    return lat.reshape(*lead, d_c), rope.reshape(*lead, d_r)
+
+
 @dataclass
 class Problem:
     """Inputs in the oracle's terms (numpy, host).

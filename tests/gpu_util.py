@@ -24,12 +24,12 @@ def to_device(w, device="cuda"):
     return q_nope, q_rope, kv, bt, seq
 
 
-def params_for(w, num_units=0, timeout_us=0, token_group=0):
+def params_for(w, num_units=0, timeout_us=0, token_group=0, qk_fp8=0):
     from mla_absorbed_decode_02_gb300 import MlaDecodeParams, MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_OUT_BF16, MLA_OUT_F32
     return MlaDecodeParams.make(w.batch, w.s_q, w.num_heads, w.num_pages, w.block_table.shape[1], causal=w.causal,
                                 kv_dtype=MLA_KV_FP8_E4M3 if w.kv_dtype == "fp8" else MLA_KV_BF16,
                                 out_dtype=MLA_OUT_F32 if w.out_dtype == "f32" else MLA_OUT_BF16,
-                                num_units=num_units, timeout_us=timeout_us, token_group=token_group)
+                                num_units=num_units, timeout_us=timeout_us, token_group=token_group, qk_fp8=qk_fp8)
 
 
 def run_gpu(w, num_units=0, token_group=0):

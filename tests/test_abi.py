@@ -65,6 +65,9 @@ def test_workspace_size_without_gpu(lib):
     (dict(s_q=2, token_group=3), _lib.MLA_ERR_INVALID_ARG),   # must divide s_q
     (dict(s_q=8, token_group=8), _lib.MLA_ERR_INVALID_ARG),   # at most 4 (clusters of 8 CTAs)
     (dict(token_group=-1), _lib.MLA_ERR_INVALID_ARG),
+    (dict(qk_fp8=1), _lib.MLA_ERR_INVALID_ARG),                # FP8 QK needs the FP8 cache
+    (dict(qk_fp8=2, kv_dtype=_lib.MLA_KV_FP8_E4M3), _lib.MLA_ERR_INVALID_ARG),
+    (dict(qk_fp8=1, kv_dtype=_lib.MLA_KV_FP8_E4M3, s_q=2, token_group=2), _lib.MLA_ERR_UNSUPPORTED),
 ])
 def test_bad_params_are_rejected(lib, kw, status):
     with pytest.raises(_lib.MlaError) as e:
@@ -87,6 +90,24 @@ def test_workspace_of_a_token_group(lib):
 
 def _a256(x):
     return (x + 255) // 256 * 256
+
+
+def test_fp8_qk_params_accepted(lib):
+    """The FP8-QK decode takes the FP8 cache and no token group; its buffers are those of the
+    FP8 decode."""
+    kw = dict(batch=3, s_q=2, num_units=7, kv_dtype=_lib.MLA_KV_FP8_E4M3)
+    assert _lib.mla_get_workspace_size(_p(qk_fp8=1, **kw)) == _lib.mla_get_workspace_size(_p(**kw))
+    assert _lib.mla_get_workspace_size(_p(qk_fp8=1, token_group=1, **kw))
+
+
+def test_query_quantizer_rejects_bad_arguments(lib):
+    import torch
+    x = torch.zeros(1024, dtype=torch.uint8)
+    for args in ((None, x, x, 1), (x, None, x, 1), (x, x, None, 1), (x, x, x, -1)):
+        with pytest.raises(_lib.MlaError) as e:
+            _lib.mla_quantize_q_fp8(*args, stream=0)
+        assert e.value.status == _lib.MLA_ERR_INVALID_ARG
+    _lib.mla_quantize_q_fp8(x, x, x, 0, stream=0)  # no rows: nothing to launch
 
 
 def test_reserved_must_be_zero(lib):

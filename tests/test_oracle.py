@@ -322,6 +322,33 @@ def test_fp8_cache_matches_f64_cache():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+def test_fp8_rows_to_f64_matches_the_oracles_cache_decoding():
+    """oracle.fp8_rows_to_f64 (the FP8-QK query's decoding) against torch's E4M3 decode times the stored
+    scale, and against the C oracle's own decoding of the same rows as an FP8 cache: an FP8-cache
+    problem and a float64-cache problem built from fp8_rows_to_f64 of its pool give equal results."""
+    import mla_workloads as mw
+    rng = np.random.default_rng(21)
+    n = 2 * 64
+    x = (rng.standard_normal((n, 576)) * np.exp(rng.uniform(-6, 6, (n, 1)))).astype(np.float32)
+    x[5, 128:256] = 0.0  # an all-zero tile (scale 1)
+    rows = mw.quantize_fp8_rows(x[:, :512], mw.to_bf16_bits(x[:, 512:]))
+    lat, rope = oracle.fp8_rows_to_f64(rows.reshape(2, 64, 656))
+    codes = torch.from_numpy(rows[:, :512].copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    scales = rows[:, 512:528].copy().view(np.float32).astype(np.float64)
+    assert np.array_equal(lat.reshape(n, 512), codes * np.repeat(scales, 128, axis=1))
+    rope_bits = mw.to_bf16_bits(x[:, 512:])
+    assert np.array_equal(rope.reshape(n, 64),
+                          torch.from_numpy(rope_bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy())
+    assert np.all(lat.reshape(n, 512)[5, 128:256] == 0.0)
+    pool_f64 = np.concatenate([lat, rope], axis=2)
+    bt = np.array([[1, 0]], np.int32)
+    qn, qr = rng.standard_normal((1, 1, 2, 512)), rng.standard_normal((1, 1, 2, 64))
+    L = np.array([113], np.int32)
+    a = Problem(qn, qr, rows.reshape(2, 64, 656), KV_FP8, bt, L, 1 / math.sqrt(192)).full()
+    b = Problem(qn, qr, pool_f64, KV_F64, bt, L, 1 / math.sqrt(192)).full()
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
 def test_threads_match_single_thread():
     rng = np.random.default_rng(16)
     Ls = np.array([33, 64, 130, 1], np.int32)
