@@ -481,7 +481,8 @@ def run_ours(args, w, peaks, world, rank, local):
     import torch
     import mla_workloads as mw
     from mla_absorbed_decode_02_gb300.build import build
-    from mla_absorbed_decode_02_gb300 import mla_decode, mla_device_error, mla_get_scheduler_metadata
+    from mla_absorbed_decode_02_gb300 import (mla_decode, mla_device_error, mla_get_scheduler_metadata,
+                                              mla_quantize_q_fp8)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if rank == 0 or world == 1:
@@ -496,7 +497,9 @@ def run_ours(args, w, peaks, world, rank, local):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    r = time_workload(w, args.workload, peaks, args.steps, args.warmup, dev, flush, dist, args.token_group)
+    qk8 = bool(args.qk_fp8)
+    name = args.workload + ("_qk_fp8" if qk8 else "")
+    r = time_workload(w, args.workload, peaks, args.steps, args.warmup, dev, flush, dist, args.token_group, qk8)
     clk = clocks.stop()
     t_step, t_dec = r["t_step"], r["t_dec"]
     t_max = reduce_max(t_step, dist, dev)
@@ -513,6 +516,8 @@ def run_ours(args, w, peaks, world, rank, local):
     # The plan needs only the lengths: it runs on a second stream while the queries and the block
     # table cross the host link (copies are link-bound, ~200 GB/s on this host).
     plan_stream = torch.cuda.Stream(dev)
+    rows = w.batch * w.s_q * w.num_heads
+    q8 = torch.empty((rows, 656), dtype=torch.uint8, device=dev) if qk8 else None
 
     def e2e_step():
         d["seq"].copy_(hseq, non_blocking=True)
@@ -526,8 +531,12 @@ def run_ours(args, w, peaks, world, rank, local):
         d["q_rope"].copy_(hr, non_blocking=True)
         d["bt"].copy_(hbt, non_blocking=True)
         stream.wait_event(planned)
-        mla_decode(p, d["q_nope"], d["q_rope"], d["kv"], d["bt"], d["seq"], w.scale, out, lse, dec.sched,
-                   dec.workspace, stream)
+        if qk8:
+            mla_quantize_q_fp8(d["q_nope"], d["q_rope"], q8, rows, stream)
+            mla_decode(p, q8, None, d["kv"], d["bt"], d["seq"], w.scale, out, lse, dec.sched, dec.workspace, stream)
+        else:
+            mla_decode(p, d["q_nope"], d["q_rope"], d["kv"], d["bt"], d["seq"], w.scale, out, lse, dec.sched,
+                       dec.workspace, stream)
         hout.copy_(out, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
 
@@ -548,13 +557,15 @@ def run_ours(args, w, peaks, world, rank, local):
     assert mla_device_error(clear=True) == 0
     del r, host, d, dec, out, lse
 
-    flops, nbytes, row_bytes, t_roof, bound = _accounting(w, peaks)
+    flops, nbytes, row_bytes, t_roof, bound = _accounting(w, peaks, qk8)
     n = world
     value = 100.0 * n * t_roof / t_max
     res = {
         "metric": METRIC, "value": value, "unit": "% of GB300 roofline (summed over GPUs)", "n_gpus": n,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8-e4m3 cache, bf16 mma",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": ("bf16" if w.kv_dtype == "bf16" else
+                  "fp8-e4m3 cache and query, e4m3 QK mma, bf16 PV mma" if qk8 else "fp8-e4m3 cache, bf16 mma"),
         "data": "synthetic (seeded N(0,1) bf16 queries and cache, random page permutation)",
         "config": {"workload": args.workload + (f" (first {w.batch} sequences)" if args.batch else ""),
                    "batch": w.batch, "heads": w.num_heads, "s_q": w.s_q,
@@ -563,7 +574,7 @@ def run_ours(args, w, peaks, world, rank, local):
                    "l2": "flushed before every step (256 MiB write)", "parallelism": f"replicas x{n}",
                    "timing": f"median of {args.steps} steps after {args.warmup} warm-up steps, CUDA events"},
         "tflops": n * flops / t_max / 1e12, "kv_gbs": n * kv_bytes(w.seqlens, row_bytes) / t_max / 1e9,
-        "roofline": _roofline(w, args.workload, peaks, t_dec),
+        "roofline": _roofline(w, name, peaks, t_dec, qk8),
         "e2e": {"value": 100.0 * n * t_roof / t_e2e, "unit": "% of GB300 roofline (summed over GPUs)",
                 "ms_per_step": t_e2e * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "includes": "H2D q/q_rope/block_table/seqlens, scheduler metadata (second stream, "
@@ -591,7 +602,7 @@ def run_ours(args, w, peaks, world, rank, local):
         # pages, token group 2, which reads the cache once; and the opt-in FP8-QK decode)
         for name, grp, qk8 in (("uniform4k", 0, False), ("long", 0, False), ("fp8_mtp2", 0, False),
                                ("fp8_mtp2", 2, False), ("fp8_mtp2", 0, True)):
-            if name == args.workload and grp == args.token_group and not qk8:
+            if name == args.workload and grp == args.token_group and qk8 == bool(args.qk_fp8):
                 continue
             wk = mw.make_workload(WORKLOAD_INDEX[name])
             rk = time_workload(wk, name, peaks, args.steps, args.warmup, dev, flush, token_group=grp, qk_fp8=qk8)
@@ -624,6 +635,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="time the chosen workload only")
     ap.add_argument("--no-extend", action="store_true", help="skip the extend (expand path) timing")
+    ap.add_argument("--qk-fp8", action="store_true",
+                    help="FP8 cache only: the opt-in decode with QK on E4M3 codes (query quantised on the device)")
     ap.add_argument("--token-group", type=int, default=0,
                     help="new tokens per work block for the chosen workload (mla_decode_params.token_group)")
     ap.add_argument("--batch", type=int, default=0,
@@ -634,6 +647,8 @@ def main():
     world, rank, local = dist_env()
     peaks = load_peaks()
     w = mw.make_workload(WORKLOAD_INDEX[args.workload])
+    if args.qk_fp8 and (w.kv_dtype != "fp8" or args.token_group > 1):
+        ap.error("--qk-fp8 needs an FP8-cache workload and no token group")
     if args.batch:
         w = mw.first_sequences(w, args.batch)
     threads = os.cpu_count() or 1
