@@ -283,6 +283,23 @@ def test_large_logits_within_the_stated_tolerance(num_units):
     full_check(w, tol=tol, num_units=num_units, what=f"large logits x4 U={num_units}")
 
 
+def test_a_million_keys():
+    """One sequence of 2^20 cached tokens (16,384 pages, 1.2 GB) beside a 3-token one: the long one is
+    split over every unit, so each of its 2 x 76 partials goes through the combine; byte offsets into
+    the pool pass 2^30.  One head from each 32-row group, and every head of the short sequence."""
+    w = mw.make_custom([1 << 20, 3], num_heads=128, seed=91)
+    out, lse, dec = run_gpu(w)
+    assert dec.num_units >= 2
+    rng = np.random.default_rng(91)
+    items = [(0, 0, [int(g + rng.integers(0, 32)) for g in range(0, 128, 32)]), (1, 0, list(range(128)))]
+    ref = oracle_sampled(w, items, threads=THREADS)
+    got_o = np.concatenate([out[b, t, h] for (b, t), (h, _, _) in ref.items()])
+    got_l = np.concatenate([lse[b, t, h] for (b, t), (h, _, _) in ref.items()])
+    ref_o = np.concatenate([o for (_, o, _) in ref.values()])
+    ref_l = np.concatenate([l for (_, _, l) in ref.values()])
+    compare(got_o, got_l, ref_o, ref_l, BF16_TOL, "2^20 keys", out_bf16=True)
+
+
 def test_long_tail_row_garbage_is_ignored():
     """Cache rows past the sequence end inside the last page hold NaN: they must not leak."""
     w = mw.make_custom([65, 130, 1], num_heads=128, seed=19)
