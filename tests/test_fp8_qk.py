@@ -153,3 +153,22 @@ def test_full_size_fp8_mtp2_sampled():
     ref_o = np.concatenate([o for (h, o, _) in res.values()])
     ref_l = np.concatenate([l for (h, _, l) in res.values()])
     compare(got_o, got_l, ref_o, ref_l, QK8_TOL, "fp8_mtp2 qk sampled", out_bf16=True, raw=True)
+
+
+def test_allocation_free_entry_point_gives_the_same_bits():
+    """mla_decode_noalloc with qk_fp8 runs the same kernels on the same plan as the buffered call."""
+    import torch
+    from mla_absorbed_decode_02_gb300 import mla_decode_noalloc, mla_device_error
+    from gpu_util import to_device
+    w = mw.make_custom([33, 700, 1400], num_heads=128, s_q=2, kv_dtype="fp8", seed=89)
+    q8 = mw.quantize_query_fp8(w)
+    ref_out, ref_lse = run_qk8(w, q8, num_units=76)
+    _, _, kv, bt, seq = to_device(w)
+    q = torch.from_numpy(np.ascontiguousarray(q8)).cuda()
+    out = torch.empty((w.batch, w.s_q, w.num_heads, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.batch, w.s_q, w.num_heads), dtype=torch.float32, device="cuda")
+    mla_decode_noalloc(params_for(w, num_units=76, qk_fp8=1), q, None, kv, bt, seq, w.scale, out, lse)
+    torch.cuda.synchronize()
+    assert mla_device_error(clear=True) == 0
+    assert np.array_equal(out.float().cpu().numpy().astype(np.float64), ref_out)
+    assert np.array_equal(lse.cpu().numpy().astype(np.float64), ref_lse)
