@@ -33,11 +33,11 @@ __device__ __forceinline__ void raise_abort(const WaitCtx& w, int site) {
   if (w.abort_peer) asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(w.abort_peer), "r"(1) : "memory");
 }
 
-// Bounded wait by one thread (the slow path).  Returns false if the CTA is
-// aborting or the wait ran out (then it raises the abort for this CTA and its
-// peer).
-template <bool kClusterScope>
-__device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
+// Bounded wait by one thread (the slow path, out of line).  Returns false if
+// the CTA is aborting or the wait ran out (then it raises the abort for this
+// CTA and its peer).
+template <bool kClusterScope = false>
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
   auto poll = [&]() { return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
@@ -52,25 +52,17 @@ __device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity, const W
   }
 }
 
-// The slow path out of line (it keeps the callers' instruction streams short).
-template <bool kClusterScope>
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
-  return wait_poll<kClusterScope>(bar, parity, w, site);
-}
-
-// Bounded wait by one thread: one inline poll, then the slow path -- inline with kInlineSlow
-// (a kernel that re-splits its registers between warpgroups makes no calls: its warps run
-// under different register counts).
-template <bool kClusterScope = false, bool kInlineSlow = false>
+// Bounded wait by one thread: one inline poll, then the slow path.
+template <bool kClusterScope = false>
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
   if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-  return kInlineSlow ? wait_poll<kClusterScope>(bar, parity, w, site) : wait_slow<kClusterScope>(bar, parity, w, site);
+  return wait_slow<kClusterScope>(bar, parity, w, site);
 }
 
 // Bounded wait by a whole warp; the result is the same in every lane.
-template <bool kClusterScope = false, bool kInlineSlow = false>
+template <bool kClusterScope = false>
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
-  const bool ok = wait_one<kClusterScope, kInlineSlow>(bar, parity, w, site);
+  const bool ok = wait_one<kClusterScope>(bar, parity, w, site);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -49,11 +49,10 @@
 // tile).  QK runs on the E4M3 codes straight from the stage (tcgen05.mma
 // kind::f8f6f4): one fp32 accumulator per 128-dim tile of this CTA's half and
 // one for the RoPE part (bf16), combined by the softmax warpgroups with the
-// query and key tile scales.  PV still needs the bf16 latent, so every page is
-// expanded after its QK has read the codes -- by a fourth warpgroup (warps
-// 12..15, 512 threads; the register file is re-split after the set-up, 176 a
-// thread for the softmax warpgroups and 80 for the others).  Tensor memory then
-// holds one score buffer (three accumulators), not two.
+// query and key tile scales.  PV still needs the bf16 latent, so the softmax
+// warpgroup of tile t expands page t once it has published P(t) (QK(t) has read
+// the codes by then, and it has read the key scales), and PV(t) waits for that.
+// Tensor memory then holds one score buffer (three accumulators), not two.
 #pragma once
 #include <type_traits>
 
@@ -62,10 +61,6 @@
 namespace mla {
 
 constexpr int kThreads = 384;
-constexpr int kThreadsQk8 = 512;                    // FP8 QK: + the expansion warpgroup
-constexpr int kRegsSoftmax = 176, kRegsOther = 80;  // FP8 QK: registers a thread after the re-split
-static_assert(2 * 4 * kRegsSoftmax + 2 * 4 * kRegsOther == 16 * (65536 / kThreadsQk8),
-              "the re-split hands out exactly the registers the 512-thread launch holds");
 constexpr int kRows = 128;      // MMA M: head rows (H <= 128, padded with zero queries)
 constexpr int kTileTok = 64;    // tokens per work tile (one page)
 #ifndef MLA_STAGES
@@ -128,8 +123,7 @@ enum : uint32_t {
   B_ML = B_X_FREE + 2,              // [parity] running max / row sum of tile t published
   B_TI_FULL = B_ML + 2,             // [t mod 8] tile-schedule entry of tile t published
   B_KV_SHARED = B_TI_FULL + kTiRing, // + stage: (token groups, loading CTA) every pair's PV(t) done
-  B_SCL_READ = B_KV_SHARED + kStages, // + stage: (FP8 QK) the softmax read the key scales; QK(t) done
-  kNumBars = B_SCL_READ + kStages
+  kNumBars = B_KV_SHARED + kStages
 };
 constexpr uint32_t OFF_TMEM_SLOT = kNumBars * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 4;
@@ -297,18 +291,6 @@ __device__ __forceinline__ uint32_t prmt_sext(uint32_t x, uint32_t s) {
   return d;
 }
 
-// Named barrier bar_id over the 128 threads of a warpgroup that also ANDs a flag across them.
-__device__ __forceinline__ bool bar_and_128(uint32_t bar_id, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, %2, 128, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(bar_id)
-      : "memory");
-  return r != 0;
-}
-
 // FP8 cache: this warpgroup thread's share of a stage (i in [0, 128): row i % 64, the 128 codes of
 // tile half i / 64) -> bf16 x tile scale, written into the 128-byte-swizzled latent layout the MMAs
 // read.  A lane takes its eight 16-code chunks starting at chunk (lane mod 8): the eight lanes of a
@@ -319,32 +301,25 @@ __device__ __forceinline__ bool bar_and_128(uint32_t bar_id, bool v) {
 // kQk8: the codes of each 128-code tile sit in the 128-byte-swizzled K-major layout the QK MMAs
 // read (logical chunk c of row r at physical chunk c ^ (r mod 8)); a lane walks logical chunks
 // ((j + lane) mod 8) ^ (lane mod 8), which keeps reads and writes conflict-free.  Rows >= valid are
-// written as zeros (they must not reach PV).  `landed` says whether this thread's warp saw the
-// codes arrive; unless every warp did, nothing is written and the result is false.
+// written as zeros (they must not reach PV).
 template <bool kQk8>
-__device__ __forceinline__ bool expand_fp8_stage(uint32_t sbase, int i, uint32_t half, uint32_t bar_id,
-                                                 bool landed = true, int valid = 64) {
+__device__ __forceinline__ void expand_fp8_stage(uint32_t sbase, int i, uint32_t half, uint32_t bar_id,
+                                                 int valid = 64) {
   const int row = i & 63, part = i >> 6;
   const uint32_t rot = (uint32_t)i & 7;
   auto lchunk = [&](int j) -> uint32_t { return kQk8 ? (((uint32_t)j + rot) & 7) ^ rot : ((uint32_t)j + rot) & 7; };
   uint32_t c[32];  // c[4j .. 4j+3]: codes of logical chunk lchunk(j)
-  float scale = 0.f;
-  if (landed) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t addr = kQk8 ? sbase + kStageCodes + part * 8192 + row * 128 + ((lchunk(j) ^ (uint32_t)(row & 7)) << 4)
-                                 : sbase + kStageCodes + row * 256 + part * 128 + 16 * lchunk(j);
-      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                   : "=r"(c[4 * j]), "=r"(c[4 * j + 1]), "=r"(c[4 * j + 2]), "=r"(c[4 * j + 3])
-                   : "r"(addr));
-    }
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(scale) : "r"(sbase + kStageScales + row * 16 + (2 * half + part) * 4));
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t addr = kQk8 ? sbase + kStageCodes + part * 8192 + row * 128 + ((lchunk(j) ^ (uint32_t)(row & 7)) << 4)
+                               : sbase + kStageCodes + row * 256 + part * 128 + 16 * lchunk(j);
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(c[4 * j]), "=r"(c[4 * j + 1]), "=r"(c[4 * j + 2]), "=r"(c[4 * j + 3])
+                 : "r"(addr));
   }
-  if (kQk8) {
-    if (!bar_and_128(bar_id, landed)) return false;
-  } else {
-    asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
-  }
+  float scale;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(scale) : "r"(sbase + kStageScales + row * 16 + (2 * half + part) * 4));
+  asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
   // E4M3 -> bf16 without the conversion units: a code's 7 magnitude bits placed as a bf16's
   // exponent and mantissa give the code's value times 2^-120 exactly (subnormal codes land on
   // bf16 subnormals), the sign bit goes to bit 15; then x 2^120 (exact) and x scale (rounded
@@ -376,16 +351,6 @@ __device__ __forceinline__ bool expand_fp8_stage(uint32_t sbase, int i, uint32_t
                                                               ((chunk ^ (uint32_t)(row & 7)) << 4)),
                  "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]));
   }
-  return true;
-}
-
-template <int kRegs>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-template <int kRegs>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
 __device__ __forceinline__ void mma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -446,7 +411,6 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
     }
     for (int i = 0; i < kTiRing; ++i) mbar_init(bar(B_TI_FULL + i), 1);
     for (int s = 0; s < kStages; ++s) mbar_init(bar(B_KV_SHARED + s), grp);  // one PV commit per pair
-    for (int s = 0; s < kStages; ++s) mbar_init(bar(B_SCL_READ + s), 4);     // the softmax warpgroup's warps
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -513,227 +477,221 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
     while (pw.next(pc)) n += pc.t1 - pc.t0;
     return n;
   };
-  if (warp < 4) {
-    // (FP8 QK: the register re-split takes whole warpgroups, converged, each at one instruction
-    // that comes before all of that warpgroup's code)
-    if (kQk8) regs_dec<kRegsOther>();
-    if (warp == 0) {
-      // ================================================================ TMA producer
-      if (lane == 0) {
-        const uint64_t pol_kv = l2_policy_evict_first();
-        const uint64_t pol_q = l2_policy_evict_last();
-        // one page into stage st: the half of its 64 rows this CTA owns
-        auto load_page = [&](uint32_t st, int page) {
-          const uint32_t sbase = base + st * kStageBytes;
-          if (kFp8) {  // 656-byte rows: codes of this half, its RoPE half, the 4 tile scales
-            mbar_arrive_expect_tx(bar(B_KV_FULL + st), kFp8StageTx);
-            if (kQk8) {  // the half's two 128-code tiles, each in the swizzled K-major layout QK reads
-              tma_load_2d(sbase + kStageCodes, &args.map_kvc, bar(B_KV_FULL + st), 256 * half, page * 64, pol_kv);
-              tma_load_2d(sbase + kStageCodes + 8192, &args.map_kvc, bar(B_KV_FULL + st), 256 * half + 128, page * 64,
-                          pol_kv);
-            } else {
-              tma_load_2d(sbase + kStageCodes, &args.map_kvc, bar(B_KV_FULL + st), 256 * half, page * 64, pol_kv);
-            }
-            tma_load_2d(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 528 + 64 * half, page * 64, pol_kv);
-            tma_load_2d(sbase + kStageScales, &args.map_kvs, bar(B_KV_FULL + st), 512, page * 64, pol_kv);
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_policy_evict_first();
+      const uint64_t pol_q = l2_policy_evict_last();
+      // one page into stage st: the half of its 64 rows this CTA owns
+      auto load_page = [&](uint32_t st, int page) {
+        const uint32_t sbase = base + st * kStageBytes;
+        if (kFp8) {  // 656-byte rows: codes of this half, its RoPE half, the 4 tile scales
+          mbar_arrive_expect_tx(bar(B_KV_FULL + st), kFp8StageTx);
+          if (kQk8) {  // the half's two 128-code tiles, each in the swizzled K-major layout QK reads
+            tma_load_2d(sbase + kStageCodes, &args.map_kvc, bar(B_KV_FULL + st), 256 * half, page * 64, pol_kv);
+            tma_load_2d(sbase + kStageCodes + 8192, &args.map_kvc, bar(B_KV_FULL + st), 256 * half + 128, page * 64,
+                        pol_kv);
           } else {
-            mbar_arrive_expect_tx(bar(B_KV_FULL + st), kBf16StageTx);
-            for (int blk = 0; blk < 4; ++blk)
-              tma_load_2d(sbase + blk * kLatBlock, &args.map_kvc, bar(B_KV_FULL + st), 256 * half + 64 * blk, page * 64,
-                          pol_kv);
-            tma_load_2d(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 512 + 32 * half, page * 64, pol_kv);
+            tma_load_2d(sbase + kStageCodes, &args.map_kvc, bar(B_KV_FULL + st), 256 * half, page * 64, pol_kv);
           }
-        };
-        // Token groups: pair 0 loads each page half once into the same half of every pair
-        // (multicast); the other pairs only expect the bytes on their own barrier.
-        const uint16_t mc_mask = (uint16_t)(0x5555u & ((1u << (2 * grp)) - 1u)) << half;
-        auto load_page_group = [&](uint32_t st, int page) {
-          const uint32_t sbase = base + st * kStageBytes;
-          if (kFp8) {
-            mbar_arrive_expect_tx(bar(B_KV_FULL + st), kFp8StageTx);
-            if (g != 0) return;
-            tma_load_2d_mc(sbase + kStageCodes, &args.map_kvc, bar(B_KV_FULL + st), 256 * half, page * 64, mc_mask, pol_kv);
-            tma_load_2d_mc(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 528 + 64 * half, page * 64, mc_mask,
-                           pol_kv);
-            tma_load_2d_mc(sbase + kStageScales, &args.map_kvs, bar(B_KV_FULL + st), 512, page * 64, mc_mask, pol_kv);
-          } else {
-            mbar_arrive_expect_tx(bar(B_KV_FULL + st), kBf16StageTx);
-            if (g != 0) return;
-            for (int blk = 0; blk < 4; ++blk)
-              tma_load_2d_mc(sbase + blk * kLatBlock, &args.map_kvc, bar(B_KV_FULL + st), 256 * half + 64 * blk,
-                             page * 64, mc_mask, pol_kv);
-            tma_load_2d_mc(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 512 + 32 * half, page * 64, mc_mask,
-                           pol_kv);
+          tma_load_2d(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 528 + 64 * half, page * 64, pol_kv);
+          tma_load_2d(sbase + kStageScales, &args.map_kvs, bar(B_KV_FULL + st), 512, page * 64, pol_kv);
+        } else {
+          mbar_arrive_expect_tx(bar(B_KV_FULL + st), kBf16StageTx);
+          for (int blk = 0; blk < 4; ++blk)
+            tma_load_2d(sbase + blk * kLatBlock, &args.map_kvc, bar(B_KV_FULL + st), 256 * half + 64 * blk, page * 64,
+                        pol_kv);
+          tma_load_2d(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 512 + 32 * half, page * 64, pol_kv);
+        }
+      };
+      // Token groups: pair 0 loads each page half once into the same half of every pair
+      // (multicast); the other pairs only expect the bytes on their own barrier.
+      const uint16_t mc_mask = (uint16_t)(0x5555u & ((1u << (2 * grp)) - 1u)) << half;
+      auto load_page_group = [&](uint32_t st, int page) {
+        const uint32_t sbase = base + st * kStageBytes;
+        if (kFp8) {
+          mbar_arrive_expect_tx(bar(B_KV_FULL + st), kFp8StageTx);
+          if (g != 0) return;
+          tma_load_2d_mc(sbase + kStageCodes, &args.map_kvc, bar(B_KV_FULL + st), 256 * half, page * 64, mc_mask, pol_kv);
+          tma_load_2d_mc(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 528 + 64 * half, page * 64, mc_mask,
+                         pol_kv);
+          tma_load_2d_mc(sbase + kStageScales, &args.map_kvs, bar(B_KV_FULL + st), 512, page * 64, mc_mask, pol_kv);
+        } else {
+          mbar_arrive_expect_tx(bar(B_KV_FULL + st), kBf16StageTx);
+          if (g != 0) return;
+          for (int blk = 0; blk < 4; ++blk)
+            tma_load_2d_mc(sbase + blk * kLatBlock, &args.map_kvc, bar(B_KV_FULL + st), 256 * half + 64 * blk,
+                           page * 64, mc_mask, pol_kv);
+          tma_load_2d_mc(sbase + kStageRope, &args.map_kvr, bar(B_KV_FULL + st), 512 + 32 * half, page * 64, mc_mask,
+                         pol_kv);
+        }
+      };
+      // logical page lp of sequence b; a length beyond the block table is reported, and no entry
+      // past the row is read
+      auto page_of = [&](int b, int lp) {
+        if (lp >= args.max_pages) {
+          atomicCAS(&g_mla_error, 0, 1);
+          lp = args.max_pages - 1;
+        }
+        return args.block_table[(int64_t)b * args.max_pages + lp];
+      };
+      // The unit's first tile is (its first query block, its first tile): the planner makes both
+      // non-empty.  That page and the block's RoPE-query half go out straight from the unit
+      // record, before the walk over the lengths.
+      mbar_arrive_expect_tx(bar(B_QR_FULL), 8192);
+      tma_load_3d(base + SM_QR, &args.map_qr, bar(B_QR_FULL), 32 * half, 0, first_qb, pol_q);
+      if (grp == 1)
+        load_page(0, page_of(first_qb / args.s_q, walker0.tile_begin));
+      else
+        load_page_group(0, page_of(first_qb / args.s_q, walker0.tile_begin));
+      TileCursor cur;
+      cur.init(walker0);
+      TileInfo ti;
+      // bf16 cache: the block-table entry of the next tile is read one iteration ahead, so its
+      // latency overlaps the wait for a free stage (ragged decode 117.4 against 119.5 us; the FP8
+      // kernel measured 1% slower with it and reads the entry when it needs it)
+      TileCursor la = cur;
+      TileInfo tl;
+      int pg_next = -1;
+      if (!kFp8 && la.next(tl) && la.next(tl)) pg_next = page_of(tl.qb / args.s_q, tl.tile);  // tile 1
+      PieceWalker ahead = walker0;  // one piece ahead of the tile walk
+      Piece np;
+      ahead.next(np);  // piece 0
+      int next_qb = -1, prev_qb = -1, prev_split = 0;
+      uint32_t t = 0, piece_no = 0;
+      while (cur.next(ti)) {
+        if (ti.first) {
+          if (piece_no > 0) {
+            if (!wait_one(bar(B_QR_EMPTY), (piece_no - 1) & 1, wc, kSiteQEmpty)) break;
+            mbar_arrive_expect_tx(bar(B_QR_FULL), 8192);
+            tma_load_3d(base + SM_QR, &args.map_qr, bar(B_QR_FULL), 32 * half, 0, ti.qb, pol_q);
           }
-        };
-        // logical page lp of sequence b; a length beyond the block table is reported, and no entry
-        // past the row is read
-        auto page_of = [&](int b, int lp) {
-          if (lp >= args.max_pages) {
-            atomicCAS(&g_mla_error, 0, 1);
-            lp = args.max_pages - 1;
-          }
-          return args.block_table[(int64_t)b * args.max_pages + lp];
-        };
-        // The unit's first tile is (its first query block, its first tile): the planner makes both
-        // non-empty.  That page and the block's RoPE-query half go out straight from the unit
-        // record, before the walk over the lengths.
-        mbar_arrive_expect_tx(bar(B_QR_FULL), 8192);
-        tma_load_3d(base + SM_QR, &args.map_qr, bar(B_QR_FULL), 32 * half, 0, first_qb, pol_q);
-        if (grp == 1)
-          load_page(0, page_of(first_qb / args.s_q, walker0.tile_begin));
-        else
-          load_page_group(0, page_of(first_qb / args.s_q, walker0.tile_begin));
-        TileCursor cur;
-        cur.init(walker0);
-        TileInfo ti;
-        // bf16 cache: the block-table entry of the next tile is read one iteration ahead, so its
-        // latency overlaps the wait for a free stage (ragged decode 117.4 against 119.5 us; the FP8
-        // kernel measured 1% slower with it and reads the entry when it needs it)
-        TileCursor la = cur;
-        TileInfo tl;
-        int pg_next = -1;
-        if (!kFp8 && la.next(tl) && la.next(tl)) pg_next = page_of(tl.qb / args.s_q, tl.tile);  // tile 1
-        PieceWalker ahead = walker0;  // one piece ahead of the tile walk
-        Piece np;
-        ahead.next(np);  // piece 0
-        int next_qb = -1, prev_qb = -1, prev_split = 0;
-        uint32_t t = 0, piece_no = 0;
+          ++piece_no;
+          next_qb = ahead.next(np) ? np.qb : -1;
+        }
+        const uint32_t st = t % kStages, ph = (t / kStages) & 1;
+        // the stage is free: here (this CTA's PV of its last tile), or, for the loading pair of a
+        // token group, in every pair
+        if (t > 0 && !wait_one(bar((grp > 1 && g == 0 ? B_KV_SHARED : B_KV_EMPTY) + st), ph ^ 1, wc, kSiteKvEmpty))
+          break;
+        {  // the tile's schedule entry for the softmax warpgroups
+          const uint32_t e = base + SM_TI + (t % kTiRing) * 32;
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(e), "r"(ti.qb), "r"(ti.valid), "r"(ti.split),
+                       "r"((ti.first ? 1 : 0) | (ti.last ? 2 : 0))
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(e + 16), "r"((int)piece_no - 1), "r"(next_qb),
+                       "r"(prev_qb), "r"(prev_split)
+                       : "memory");
+          mbar_arrive(bar(B_TI_FULL + (t % kTiRing)));
+          prev_qb = ti.qb;
+          prev_split = ti.split;
+        }
+        if (t > 0) {  // (tile 0's page went out above)
+          const int page = kFp8 ? page_of(ti.qb / args.s_q, ti.tile) : pg_next;
+          if (grp == 1)
+            load_page(st, page);
+          else
+            load_page_group(st, page);
+          if (!kFp8 && la.next(tl)) pg_next = page_of(tl.qb / args.s_q, tl.tile);
+        }
+        ++t;
+      }
+      // Token groups: the loading pair's CTAs receive every pair's last PV commits; they stay
+      // until those arrived (the barrier phases of the last min(t, stages) tiles).
+      if (grp > 1 && g == 0 && !*abort_flag)
+        for (uint32_t k = t > kStages ? t - kStages : 0; k < t; ++k)
+          if (!wait_one(bar(B_KV_SHARED + k % kStages), (k / kStages) & 1, wc, kSiteKvEmpty)) break;
+    }
+  } else if (warp == 1 || warp == 3) {
+    // ================================================================ MMA issuers
+    // warp 1: QK(t) as soon as the page is loaded and its score buffer was read out;
+    // warp 3: PV(t) as soon as P(t) is published.  The two touch disjoint tensor
+    // memory (scores / O) and only read shared memory.
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16_f32(128, 64, 0, 0);
+      constexpr uint32_t id_pv = idesc_bf16_f32(128, 256, 0, 1);
+      TileCursor cur;
+      cur.init(walker0);
+      TileInfo ti;
+      uint32_t t = 0, piece_no = 0;
+      if (warp == 1) {
         while (cur.next(ti)) {
           if (ti.first) {
-            if (piece_no > 0) {
-              if (!wait_one<false, kQk8>(bar(B_QR_EMPTY), (piece_no - 1) & 1, wc, kSiteQEmpty)) break;
-              mbar_arrive_expect_tx(bar(B_QR_FULL), 8192);
-              tma_load_3d(base + SM_QR, &args.map_qr, bar(B_QR_FULL), 32 * half, 0, ti.qb, pol_q);
-            }
+            if (!wait_one(bar(B_QR_FULL), piece_no & 1, wc, kSiteQFull)) break;
+            if (!wait_one(bar(B_QT_FULL), piece_no & 1, wc, kSiteQFull)) break;
             ++piece_no;
-            next_qb = ahead.next(np) ? np.qb : -1;
           }
-          const uint32_t st = t % kStages, ph = (t / kStages) & 1;
-          // the stage is free: here (this CTA's PV of its last tile), or, for the loading pair of a
-          // token group, in every pair
-          if (t > 0 && !wait_one<false, kQk8>(bar((grp > 1 && g == 0 ? B_KV_SHARED : B_KV_EMPTY) + st), ph ^ 1, wc, kSiteKvEmpty))
+          const uint32_t st = t % kStages, sb = t & 1;
+          const uint32_t ready = kFp8 && !kQk8 ? B_K_READY : B_KV_FULL;  // (FP8 QK reads the codes)
+          if (!wait_one(bar(ready + st), (t / kStages) & 1, wc, kSiteKvFull)) break;
+          if (kQk8) {  // one score buffer: the previous tile's scores must have been read out
+            if (t > 0 && !wait_one(bar(B_S_EMPTY + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSiteSEmpty))
+              break;
+          } else if (!wait_one(bar(B_S_EMPTY + sb), ((t >> 1) & 1) ^ 1, wc, kSiteSEmpty)) {
             break;
-          {  // the tile's schedule entry for the softmax warpgroups
-            const uint32_t e = base + SM_TI + (t % kTiRing) * 32;
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(e), "r"(ti.qb), "r"(ti.valid), "r"(ti.split),
-                         "r"((ti.first ? 1 : 0) | (ti.last ? 2 : 0))
-                         : "memory");
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(e + 16), "r"((int)piece_no - 1), "r"(next_qb),
-                         "r"(prev_qb), "r"(prev_split)
-                         : "memory");
-            mbar_arrive(bar(B_TI_FULL + (t % kTiRing)));
-            prev_qb = ti.qb;
-            prev_split = ti.split;
           }
-          if (t > 0) {  // (tile 0's page went out above)
-            const int page = kFp8 ? page_of(ti.qb / args.s_q, ti.tile) : pg_next;
-            if (grp == 1)
-              load_page(st, page);
-            else
-              load_page_group(st, page);
-            if (!kFp8 && la.next(tl)) pg_next = page_of(tl.qb / args.s_q, tl.tile);
+          tc_fence_after();
+          const uint32_t sbase = base + st * kStageBytes;
+          if (kQk8) {
+            // each 128-code tile into its own accumulator (K = 32 codes per MMA), RoPE into a third
+            constexpr uint32_t id_qk8 = idesc_e4m3_f32(128, 64, 0, 0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_e4m3_ts(tmem + TM_S8 + 64 * (k >> 2), tmem + TM_Q8 + 8 * k,
+                          smem_desc(sbase + kStageCodes + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024, kSwizzle128B),
+                          id_qk8, (k & 3) ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+              mma_bf16_ss(tmem + TM_S8 + 128, smem_desc(base + SM_QR + 32 * k, 16, 512, kSwizzle64B),
+                          smem_desc(sbase + kStageRope + 32 * k, 16, 512, kSwizzle64B), id_qk, k > 0 ? 1u : 0u);
+          } else {
+            const uint32_t d = tmem + TM_S + 64 * sb;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)  // latent half: A = query half in tensor memory
+              mma_bf16_ts(d, tmem + TM_Q + 8 * k,
+                          smem_desc(sbase + (k >> 2) * kLatBlock + (k & 3) * 32, 16, 1024, kSwizzle128B), id_qk,
+                          k > 0 ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < 2; ++k)  // RoPE half: A = RoPE-query half in shared memory
+              mma_bf16_ss(d, smem_desc(base + SM_QR + 32 * k, 16, 512, kSwizzle64B),
+                          smem_desc(sbase + kStageRope + 32 * k, 16, 512, kSwizzle64B), id_qk, 1u);
           }
+          mma_commit(bar(B_S_FULL + sb));
+          if (ti.last) mma_commit(bar(B_QR_EMPTY));
           ++t;
         }
-        // Token groups: the loading pair's CTAs receive every pair's last PV commits; they stay
-        // until those arrived (the barrier phases of the last min(t, stages) tiles).
-        if (grp > 1 && g == 0 && !*abort_flag)
-          for (uint32_t k = t > kStages ? t - kStages : 0; k < t; ++k)
-            if (!wait_one<false, kQk8>(bar(B_KV_SHARED + k % kStages), (k / kStages) & 1, wc, kSiteKvEmpty)) break;
-      }
-    } else if (warp == 1 || warp == 3) {
-      // ================================================================ MMA issuers
-      // warp 1: QK(t) as soon as the page is loaded and its score buffer was read out;
-      // warp 3: PV(t) as soon as P(t) is published.  The two touch disjoint tensor
-      // memory (scores / O) and only read shared memory.
-      if (lane == 0) {
-        constexpr uint32_t id_qk = idesc_bf16_f32(128, 64, 0, 0);
-        constexpr uint32_t id_pv = idesc_bf16_f32(128, 256, 0, 1);
-        TileCursor cur;
-        cur.init(walker0);
-        TileInfo ti;
-        uint32_t t = 0, piece_no = 0;
-        if (warp == 1) {
-          while (cur.next(ti)) {
-            if (ti.first) {
-              if (!wait_one<false, kQk8>(bar(B_QR_FULL), piece_no & 1, wc, kSiteQFull)) break;
-              if (!wait_one<false, kQk8>(bar(B_QT_FULL), piece_no & 1, wc, kSiteQFull)) break;
-              ++piece_no;
-            }
-            const uint32_t st = t % kStages, sb = t & 1;
-            const uint32_t ready = kFp8 && !kQk8 ? B_K_READY : B_KV_FULL;  // (FP8 QK reads the codes)
-            if (!wait_one<false, kQk8>(bar(ready + st), (t / kStages) & 1, wc, kSiteKvFull)) break;
-            if (kQk8) {  // one score buffer: the previous tile's scores must have been read out
-              if (t > 0 && !wait_one<false, kQk8>(bar(B_S_EMPTY + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSiteSEmpty))
-                break;
-            } else if (!wait_one<false, kQk8>(bar(B_S_EMPTY + sb), ((t >> 1) & 1) ^ 1, wc, kSiteSEmpty)) {
-              break;
-            }
-            tc_fence_after();
-            const uint32_t sbase = base + st * kStageBytes;
-            if (kQk8) {
-              // each 128-code tile into its own accumulator (K = 32 codes per MMA), RoPE into a third
-              constexpr uint32_t id_qk8 = idesc_e4m3_f32(128, 64, 0, 0);
+      } else {
+        while (cur.next(ti)) {
+          const uint32_t pb = t & 1, st = t % kStages;
+          if (!wait_one(bar(B_P_FULL + pb), (t >> 1) & 1, wc, kSitePFull)) break;
+          // FP8 QK: the page's bf16 latent (V) is written after its QK, by the expansion warpgroup
+          if (kQk8 && !wait_one(bar(B_K_READY + st), (t / kStages) & 1, wc, kSiteKvFull)) break;
+          tc_fence_after();
+          const uint32_t sbase = base + st * kStageBytes;
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
-                mma_e4m3_ts(tmem + TM_S8 + 64 * (k >> 2), tmem + TM_Q8 + 8 * k,
-                            smem_desc(sbase + kStageCodes + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024, kSwizzle128B),
-                            id_qk8, (k & 3) ? 1u : 0u);
-#pragma unroll
-              for (int k = 0; k < 2; ++k)
-                mma_bf16_ss(tmem + TM_S8 + 128, smem_desc(base + SM_QR + 32 * k, 16, 512, kSwizzle64B),
-                            smem_desc(sbase + kStageRope + 32 * k, 16, 512, kSwizzle64B), id_qk, k > 0 ? 1u : 0u);
-            } else {
-              const uint32_t d = tmem + TM_S + 64 * sb;
-#pragma unroll
-              for (int k = 0; k < 16; ++k)  // latent half: A = query half in tensor memory
-                mma_bf16_ts(d, tmem + TM_Q + 8 * k,
-                            smem_desc(sbase + (k >> 2) * kLatBlock + (k & 3) * 32, 16, 1024, kSwizzle128B), id_qk,
-                            k > 0 ? 1u : 0u);
-#pragma unroll
-              for (int k = 0; k < 2; ++k)  // RoPE half: A = RoPE-query half in shared memory
-                mma_bf16_ss(d, smem_desc(base + SM_QR + 32 * k, 16, 512, kSwizzle64B),
-                            smem_desc(sbase + kStageRope + 32 * k, 16, 512, kSwizzle64B), id_qk, 1u);
-            }
-            mma_commit(bar(B_S_FULL + sb));
-            if (ti.last) mma_commit(bar(B_QR_EMPTY));
-            ++t;
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t a = smem_desc(base + SM_P + pb * kPBytes + k * 4096, 2048, 128, kSwizzleNone);
+            const uint64_t bv = smem_desc(sbase + k * 2048, kLatBlock, 1024, kSwizzle128B);
+            mma_bf16_ss(tmem + TM_O, a, bv, id_pv, (!ti.first || k > 0) ? 1u : 0u);
           }
-        } else {
-          while (cur.next(ti)) {
-            const uint32_t pb = t & 1, st = t % kStages;
-            if (!wait_one<false, kQk8>(bar(B_P_FULL + pb), (t >> 1) & 1, wc, kSitePFull)) break;
-            // FP8 QK: the page's bf16 latent (V) is written after its QK, by the expansion warpgroup
-            if (kQk8 && !wait_one<false, kQk8>(bar(B_K_READY + st), (t / kStages) & 1, wc, kSiteKvFull)) break;
-            tc_fence_after();
-            const uint32_t sbase = base + st * kStageBytes;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t a = smem_desc(base + SM_P + pb * kPBytes + k * 4096, 2048, 128, kSwizzleNone);
-              const uint64_t bv = smem_desc(sbase + k * 2048, kLatBlock, 1024, kSwizzle128B);
-              mma_bf16_ss(tmem + TM_O, a, bv, id_pv, (!ti.first || k > 0) ? 1u : 0u);
-            }
-            mma_commit(bar(B_KV_EMPTY + st));
-            if (grp > 1) mma_commit_mc(bar(B_KV_SHARED + st), (uint16_t)(1u << half));  // the loading CTA
-            mma_commit(bar(B_P_FREE + pb));
-            ++t;
-          }
+          mma_commit(bar(B_KV_EMPTY + st));
+          if (grp > 1) mma_commit_mc(bar(B_KV_SHARED + st), (uint16_t)(1u << half));  // the loading CTA
+          mma_commit(bar(B_P_FREE + pb));
+          ++t;
         }
-        // no MMA of this issuer may still run when tensor memory is released
-        const uint32_t drain = bar(warp == 1 ? B_DRAIN : B_DRAIN_PV);
-        mma_commit(drain);
-        WaitCtx wd = wc;
-        wd.timeout_ns = 100000000ull;
-        volatile int no_abort = 0;
-        wd.abort_local = &no_abort;
-        wd.abort_peer = 0;
-        wait_one<false, kQk8>(drain, 0, wd, kSiteDrain);
       }
+      // no MMA of this issuer may still run when tensor memory is released
+      const uint32_t drain = bar(warp == 1 ? B_DRAIN : B_DRAIN_PV);
+      mma_commit(drain);
+      WaitCtx wd = wc;
+      wd.timeout_ns = 100000000ull;
+      volatile int no_abort = 0;
+      wd.abort_local = &no_abort;
+      wd.abort_peer = 0;
+      wait_one(drain, 0, wd, kSiteDrain);
     }
-  } else if (!kQk8 || warp < 12) {
+  } else if (warp >= 4) {
     // ================================================================ softmax warpgroups
-    if (kQk8) regs_inc<kRegsSoftmax>();
     const uint32_t w = (uint32_t)(warp - 4) >> 2;  // this warpgroup owns the tiles of parity w
     const int r = ((warp & 3) << 5) | lane;        // head row == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -944,7 +902,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
     const uint32_t n_tiles = count_tiles();
     auto expand_tile = [&](uint32_t tt) -> bool {
       const uint32_t st = tt % kStages;
-      if (!wait_warp<false, kQk8>(bar(B_KV_FULL + st), (tt / kStages) & 1, wc, kSiteKvFull)) return false;
+      if (!wait_warp(bar(B_KV_FULL + st), (tt / kStages) & 1, wc, kSiteKvFull)) return false;
       expand_fp8_stage<false>(base + st * kStageBytes, r, half, 1 + w);
       fence_proxy_async_smem();
       __syncwarp();
@@ -992,7 +950,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
       constexpr bool kFull = decltype(full)::value;
           const uint32_t sb = w, ph = (t >> 1) & 1;
           // ---- own partial scores; the score buffer is free again right after the read
-          if (!(ok = wait_warp<false, kQk8>(bar(B_S_FULL + sb), ph, wc, kSiteSFull))) return false;
+          if (!(ok = wait_warp(bar(B_S_FULL + sb), ph, wc, kSiteSFull))) return false;
           tc_fence_after();
           // QK(t) is done: if it was the piece's last, the query half in tensor memory is free.  From
           // tile 2 on, this warpgroup's buffer (P(t-2), read by PV(t-2)) is not handed back for X(t)
@@ -1002,7 +960,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
             if (t < 2) {
               load_q_tmem(np_qb);
             } else {
-              if (!(ok = wait_warp<false, kQk8>(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) return false;
+              if (!(ok = wait_warp(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) return false;
               load_q_tmem_staged(np_qb);
               if (lane == 0) mbar_arrive_remote(peer_bar0 + 8 * (B_X_FREE + sb));
               handed_back = true;
@@ -1012,10 +970,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           float beta = 0.f;  // bias the block-float decode leaves on every score of the row
           if constexpr (kQk8) {
             // partial score = sq_0 sk_0 S_0 + sq_1 sk_1 S_1 + S_R, 16 columns at a time; the key scales
-            // (this half's two of each row's four) are read from the stage, which the expansion
-            // warpgroup overwrites once B_SCL_READ says they are read
+            // (this half's two of each row's four) are read from the stage, which this warpgroup
+            // overwrites with the page's bf16 latent after P(t)
             const uint32_t st = t % kStages;
-            if (!(ok = wait_warp<false, kQk8>(bar(B_KV_FULL + st), (t / kStages) & 1, wc, kSiteKvFull))) return false;
+            if (!(ok = wait_warp(bar(B_KV_FULL + st), (t / kStages) & 1, wc, kSiteKvFull))) return false;
             const uint32_t scl = base + st * kStageBytes + kStageScales + 8 * half;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -1040,10 +998,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-              mbar_arrive(bar(B_S_EMPTY + sb));
-              mbar_arrive(bar(B_SCL_READ + st));
-            }
+            if (lane == 0) mbar_arrive(bar(B_S_EMPTY + sb));
           } else {
             uint32_t v0[32], v1[32];
             tmem_ld32(tmem + lane_off + TM_S + 64 * sb, v0);
@@ -1061,7 +1016,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           // this warpgroup's buffer held P(t-2): hand it back to the peer once PV(t-2) is done
           // (a relaxed arrive, made to depend on the values read from the buffer)
           if (t >= 2 && !handed_back) {
-            if (!(ok = wait_warp<false, kQk8>(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) return false;
+            if (!(ok = wait_warp(bar(B_P_FREE + sb), ph ^ 1, wc, kSitePEmpty))) return false;
             if (lane == 0) mbar_arrive_remote_relaxed(peer_bar0 + 8 * (B_X_FREE + sb), slot_dep);
           }
           const int valid = x.valid;
@@ -1078,7 +1033,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
             }
             const int e = bfp_exponent(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])));
             const uint64_t k = splat_f32x2(pow2f(14 - e));
-            if (!(ok = wait_warp<false, kQk8>(bar(B_X_FREE + sb), ph ^ 1, wc, kSiteXFree))) return false;
+            if (!(ok = wait_warp(bar(B_X_FREE + sb), ph ^ 1, wc, kSiteXFree))) return false;
             const uint32_t full = peer_bar0 + 8 * (B_X_FULL + sb);
   #pragma unroll
             for (int j = 0; j < 8; ++j)  // each 16-byte chunk goes out as soon as it is encoded
@@ -1088,7 +1043,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           }
           // ---- the peer's half of the same scores
           if ((warp & 3) == 0 && lane == 0) mbar_arrive_expect_tx(bar(B_X_FULL + sb), kXBytes);
-          if (!(ok = wait_warp<true, kQk8>(bar(B_X_FULL + sb), ph, wc, kSiteXFull))) return false;
+          if (!(ok = wait_warp<true>(bar(B_X_FULL + sb), ph, wc, kSiteXFull))) return false;
           {
             uint32_t pe;
             asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pe) : "r"(my_xe + r * 4));
@@ -1128,7 +1083,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           // ---- running max: decided from the previous tile's (the other warpgroup's)
           float m_prev = 0.f, l_other = 0.f;
           if (t > 0) {
-            if (!(ok = wait_warp<false, kQk8>(bar(B_ML + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSiteML))) return false;
+            if (!(ok = wait_warp(bar(B_ML + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSiteML))) return false;
             m_prev = ml[((sb ^ 1) * 2) * kRows + r];
             l_other = ml[((sb ^ 1) * 2 + 1) * kRows + r];
           }
@@ -1148,7 +1103,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           // once every thread has read its exchange data from it; P(t) goes there afterwards
           if (kFull && epi_pending) {
             asm volatile("bar.sync %0, 128;" ::"r"(1 + w) : "memory");
-            if (!(ok = wait_warp<false, kQk8>(bar(B_P_FREE + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSitePEmpty))) return false;
+            if (!(ok = wait_warp(bar(B_P_FREE + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSitePEmpty))) return false;
             tc_fence_after();
             epilogue(m_prev, epi_l, 0, 1);
             epi_pending = false;
@@ -1193,7 +1148,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           if (lane == 0) mbar_arrive(bar(B_ML + sb));
           // ---- a raised running max rescales O (after PV(t-1), before PV(t))
           if (__any_sync(0xffffffffu, alpha != 1.f)) {
-            if (!(ok = wait_warp<false, kQk8>(bar(B_P_FREE + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSitePEmpty))) return false;
+            if (!(ok = wait_warp(bar(B_P_FREE + (sb ^ 1)), ((t - 1) >> 1) & 1, wc, kSitePEmpty))) return false;
             tc_fence_after();
   #pragma unroll 1
             for (int c = 0; c < 8; ++c) {
@@ -1223,12 +1178,20 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_P_FULL + sb));
+          if (kQk8) {  // FP8 QK: this tile's page to bf16 for PV(t) (QK(t) has read the codes, this
+                       // warpgroup the key scales)
+            const uint32_t st = t % kStages;
+            expand_fp8_stage<true>(base + st * kStageBytes, r, half, 1 + w, valid);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_K_READY + st));
+          }
           if (kFp8 && !kQk8 && t + 3 < n_tiles && !(ok = expand_tile(t + 3))) return false;
       return true;
     };
     // this warpgroup's tiles: t = w, w + 2, ...
     for (t = w; ok && t < n_tiles; t += 2) {
-      if (!(ok = wait_warp<false, kQk8>(bar(B_TI_FULL + (t % kTiRing)), (t / kTiRing) & 1, wc, kSiteSFull))) break;
+      if (!(ok = wait_warp(bar(B_TI_FULL + (t % kTiRing)), (t / kTiRing) & 1, wc, kSiteSFull))) break;
       read_entry(t);
       if (kQk8 && x.qb != sq_qb) {  // this row's two query tile scales (of this half) for the tile's token
         sq_qb = x.qb;
@@ -1265,7 +1228,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
     // the unit's last tile n_tiles-1 (its entry is still in the ring): its piece ends the unit
     t = n_tiles;
     if (ok && t > 0) {
-      if (!(ok = wait_warp<false, kQk8>(bar(B_TI_FULL + ((t - 1) % kTiRing)), ((t - 1) / kTiRing) & 1, wc, kSiteSFull))) t = 0;
+      if (!(ok = wait_warp(bar(B_TI_FULL + ((t - 1) % kTiRing)), ((t - 1) / kTiRing) & 1, wc, kSiteSFull))) t = 0;
       const bool pend = epi_pending;
       read_entry(t - 1);
       epi_pending = pend;
@@ -1287,34 +1250,15 @@ __device__ __forceinline__ void decode_body(const DecodeArgs& args) {
         const uint32_t po = pp ^ 1;
         l_tot = l_mine + (x.first ? 0.f : ml[(po * 2 + 1) * kRows + r] * exp2f(ml[(po * 2) * kRows + r] - m_fin));
       } else {  // epi_pending: the other warpgroup's tile t-1 ended the piece
-        go = wait_warp<false, kQk8>(bar(B_ML + pp), ((t - 1) >> 1) & 1, wc, kSiteML);
+        go = wait_warp(bar(B_ML + pp), ((t - 1) >> 1) & 1, wc, kSiteML);
         m_fin = ml[(pp * 2) * kRows + r];
         const float l_other = ml[(pp * 2 + 1) * kRows + r];
         l_tot = l_other + (my_piece == epi_piece ? l_mine * exp2f(m_ref - m_fin) : 0.f);
       }
-      if (go && wait_warp<false, kQk8>(bar(B_P_FREE + pp), ((t - 1) >> 1) & 1, wc, kSitePEmpty)) {
+      if (go && wait_warp(bar(B_P_FREE + pp), ((t - 1) >> 1) & 1, wc, kSitePEmpty)) {
         tc_fence_after();
         epilogue(m_fin, l_tot, owner ? 1 : 0, 2);
       }
-    }
-  } else if (kQk8) {
-    // ================================================================ FP8 QK: expansion warpgroup
-    // Page t after QK(t) has read its codes and the softmax its key scales (B_SCL_READ), in tile
-    // order; PV(t) waits for B_K_READY(t).  Stage t is loaded again only after PV(t), so this
-    // order waits on nothing that waits on it.
-    regs_dec<kRegsOther>();
-    const int i = tid - 12 * 32;  // [0, 128)
-    TileCursor cur;
-    cur.init(walker0);
-    TileInfo ti;
-    for (uint32_t tt = 0; cur.next(ti); ++tt) {
-      const uint32_t st = tt % kStages, ph = (tt / kStages) & 1;
-      bool landed = wait_warp<false, kQk8>(bar(B_KV_FULL + st), ph, wc, kSiteKvFull);
-      if (landed) landed = wait_warp<false, kQk8>(bar(B_SCL_READ + st), ph, wc, kSiteSFull);
-      if (!expand_fp8_stage<true>(base + st * kStageBytes, i, half, 3, landed, ti.valid)) break;
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_K_READY + st));
     }
   }
 
@@ -1347,8 +1291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_fp8_group_kernel(const __grid_constant__ DecodeArgs args) {
   decode_body<true, true>(args);
 }
-// FP8 cache with QK on the E4M3 codes (opt-in): 512 threads, one pair per new token
-__global__ void __launch_bounds__(kThreadsQk8, 1)
+// FP8 cache with QK on the E4M3 codes (opt-in): one pair per new token
+__global__ void __launch_bounds__(kThreads, 1)
     mla_decode_fp8qk_kernel(const __grid_constant__ DecodeArgs args) {
   decode_body<true, false, true>(args);
 }

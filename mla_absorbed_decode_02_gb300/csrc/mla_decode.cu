@@ -231,7 +231,6 @@ struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
   int max_clusters[5] = {0, 0, 0, 0, 0};  // [G]: clusters of 2G decode CTAs that fit at once
-  bool qk8_ok = false;                    // the FP8-QK kernel's register count allows its re-split
 };
 std::mutex g_mu;
 DeviceInfo g_dev[64];
@@ -249,12 +248,6 @@ int32_t device_info(DeviceInfo** out) {
                           (const void*)mla_decode_fp8qk_kernel})
       if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
         return MLA_ERR_CUDA;
-    {  // the FP8-QK kernel re-splits its registers between warpgroups: the launch must hold at least
-       // what the re-split hands out, or a warpgroup's request would wait forever
-      cudaFuncAttributes fa;
-      if (cudaFuncGetAttributes(&fa, (const void*)mla_decode_fp8qk_kernel) != cudaSuccess) return MLA_ERR_CUDA;
-      d.qk8_ok = fa.numRegs * 2 >= kRegsSoftmax + kRegsOther;
-    }
     for (int G = 1; G <= 4; ++G) {  // GPCs hold whole clusters: bigger ones leave SMs idle
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * G * (d.sm_count / (2 * G)), 1, 1);
@@ -511,7 +504,6 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
   if (!std::isfinite(scale) || !(scale > 0.f)) return MLA_ERR_INVALID_ARG;  // the kernel takes row maxima before scaling
   DeviceInfo* dinfo = nullptr;
   if ((st = device_info(&dinfo)) != MLA_OK) return st;
-  if (qk8 && !dinfo->qk8_ok) return MLA_ERR_CUDA;
   int32_t U = 0;
   if ((st = resolve_units(p, &U)) != MLA_OK) return st;
   const int H = p->num_heads, NQB = p->batch * p->s_q, G = resolve_group(p);
@@ -549,7 +541,7 @@ int32_t mla_decode_splitkv(const mla_decode_params* p, const void* q_nope_absorb
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * G * U, 1, 1);
-  cfg.blockDim = dim3(qk8 ? kThreadsQk8 : kThreads, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = static_cast<cudaStream_t>(stream);
   // one unit = a cluster of 2G CTAs; programmatic dependent launch: the kernel's set-up
