@@ -319,6 +319,13 @@ def _roofline(w, name, peaks, t_dec, qk8=False):
     return roof
 
 
+class _NoFlush:
+    """Stands in for the flush buffer when the decode is timed without flushing L2."""
+
+    def zero_(self):
+        pass
+
+
 def time_workload(w, name, peaks, steps, warmup, dev, flush, dist=None, token_group=0, qk_fp8=False):
     """Device timing of one workload, inputs resident in HBM, L2 flushed before every step.
 
@@ -492,6 +499,10 @@ def run_ours(args, w, peaks, world, rank, local):
         dist.barrier()
         build()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # > L2 (129 MB)
+    # The decode's inputs (the cache: 151 MB to 845 MB) are larger than L2; --l2 none times the
+    # decode steps without the flush.  The projections and the extend always flush (their weights
+    # fit in L2).
+    flush_dec = _NoFlush() if args.l2 == "none" else flush
     stream = torch.cuda.current_stream(dev)
 
     clocks = ClockSampler(local)
@@ -499,7 +510,7 @@ def run_ours(args, w, peaks, world, rank, local):
     time.sleep(0.3)
     qk8 = bool(args.qk_fp8)
     name = args.workload + ("_qk_fp8" if qk8 else "")
-    r = time_workload(w, args.workload, peaks, args.steps, args.warmup, dev, flush, dist, args.token_group, qk8)
+    r = time_workload(w, args.workload, peaks, args.steps, args.warmup, dev, flush_dec, dist, args.token_group, qk8)
     clk = clocks.stop()
     t_step, t_dec = r["t_step"], r["t_dec"]
     t_max = reduce_max(t_step, dist, dev)
@@ -541,12 +552,12 @@ def run_ours(args, w, peaks, world, rank, local):
         hlse.copy_(lse, non_blocking=True)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_dec.zero_()
         e2e_step()
     torch.cuda.synchronize(dev)
     e_ms = []
     for _ in range(args.steps):
-        flush.zero_()
+        flush_dec.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         e2e_step()
@@ -571,7 +582,9 @@ def run_ours(args, w, peaks, world, rank, local):
                    "batch": w.batch, "heads": w.num_heads, "s_q": w.s_q,
                    "seqlens": f"{int(w.seqlens.min())}..{int(w.seqlens.max())} (sum {int(w.seqlens.sum())})",
                    "kv_dtype": w.kv_dtype, "pages": w.num_pages, "units": units, "token_group": args.token_group or 1,
-                   "l2": "flushed before every step (256 MiB write)", "parallelism": f"replicas x{n}",
+                   "l2": (f"not flushed: the cache ({kv_bytes(w.seqlens, row_bytes) / 1e6:.0f} MB) is larger than "
+                          "L2 (129 MB)" if args.l2 == "none"
+                          else "flushed before every step (256 MiB write)"), "parallelism": f"replicas x{n}",
                    "timing": f"median of {args.steps} steps after {args.warmup} warm-up steps, CUDA events"},
         "tflops": n * flops / t_max / 1e12, "kv_gbs": n * kv_bytes(w.seqlens, row_bytes) / t_max / 1e9,
         "roofline": _roofline(w, name, peaks, t_dec, qk8),
@@ -605,7 +618,7 @@ def run_ours(args, w, peaks, world, rank, local):
             if name == args.workload and grp == args.token_group and qk8 == bool(args.qk_fp8):
                 continue
             wk = mw.make_workload(WORKLOAD_INDEX[name])
-            rk = time_workload(wk, name, peaks, args.steps, args.warmup, dev, flush, token_group=grp, qk_fp8=qk8)
+            rk = time_workload(wk, name, peaks, args.steps, args.warmup, dev, flush_dec, token_group=grp, qk_fp8=qk8)
             _, _, _, tr, _ = _accounting(wk, peaks, qk8)
             key = name + (f"_token_group{grp}" if grp else "") + ("_qk_fp8" if qk8 else "")
             per[key] = {
@@ -635,6 +648,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="time the chosen workload only")
     ap.add_argument("--no-extend", action="store_true", help="skip the extend (expand path) timing")
+    ap.add_argument("--l2", default="flush", choices=["flush", "none"],
+                    help="flush L2 before every decode step (256 MiB write), or not (the cache is larger than L2)")
     ap.add_argument("--qk-fp8", action="store_true",
                     help="FP8 cache only: the opt-in decode with QK on E4M3 codes (query quantised on the device)")
     ap.add_argument("--token-group", type=int, default=0,
