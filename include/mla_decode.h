@@ -91,7 +91,7 @@ typedef struct mla_decode_params {
                                 cluster of 2G CTAs, pages multicast to every pair); 1..4 and dividing
                                 s_q; 0 = 1.  Clusters of 4 / 8 CTAs occupy 144 / 120 of GB300's 152 SMs,
                                 so G > 1 pays where DRAM, not the SMs, bounds the decode */
-  int32_t qk_fp8;            /* FP8 cache only, opt-in: nonzero => QK runs on E4M3 codes on the FP8 tensor
+  int32_t qk_fp8;            /* FP8 cache only, opt-in (0 or 1): 1 => QK runs on E4M3 codes on the FP8 tensor
                                 cores ("MLA inference: two computation paths and FlashMLA", exercise 2
                                 "An FP8 KV cache").  The query is then passed quantised like the cache:
                                 q_nope_absorbed points to [B][s_q][H][656 bytes] rows written by
