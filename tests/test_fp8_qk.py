@@ -104,6 +104,16 @@ def test_fewer_heads_and_f32_output():
     full_check(w, num_units=3, what="fp8 qk H=40 f32")
 
 
+def test_empty_and_short_sequences():
+    """Sequences of no key and sequences shorter than s_q (tokens that see no key: out = 0, lse = -inf)."""
+    w = mw.make_custom([0, 100, 0, 1, 3], num_heads=32, s_q=4, kv_dtype="fp8", seed=90)
+    q8 = mw.quantize_query_fp8(w)
+    out, lse = run_qk8(w, q8, num_units=3)
+    ref_out, ref_lse = _oracle_problem(w, q8).full(threads=THREADS)
+    compare(out, lse, ref_out, ref_lse, QK8_TOL, "fp8 qk empty and short", out_bf16=True)
+    assert np.all(lse[0] == -np.inf) and np.all(out[0] == 0) and np.all(lse[2] == -np.inf)
+
+
 def test_row_garbage_past_the_end_is_ignored():
     """Rows past the sequence end hold NaN codes, NaN scales and NaN RoPE: QK reads them as codes, the
     expansion must write them as zeros and the softmax must mask their scores."""
