@@ -101,3 +101,18 @@ def test_extend_flops_match_printed_path_one(row):
     """bench.extend_flops (the extend leg's FLOP count) reproduces the printed path-one totals."""
     name, q, k, p1, _ = row
     assert close(bench.extend_flops(q, k, H) / 1e9, p1, 1), (name, bench.extend_flops(q, k, H) / 1e9, p1)
+
+
+def test_fp8_qk_tensor_peak_weights_each_contraction_by_its_rate():
+    """The FP8-QK decode's tensor roofline: per pair and head, 2*d_c FLOPs of QK on E4M3 codes at
+    twice the bf16 rate and 2*d_r (RoPE QK) + 2*d_c (PV) at the bf16 rate, so the time of a pair is
+    the sum of the two parts' times; the effective peak is FLOPs over that time."""
+    peaks = {"hbm_gbs": 1000.0, "bf16_tflops": 100.0}
+    fp8, bf16 = 2 * DC, 2 * ROPE + 2 * DC
+    t_pair = fp8 / (2 * 100.0) + bf16 / 100.0
+    assert abs(bench.qk8_tensor_peak(peaks) - (fp8 + bf16) / t_pair) < 1e-9
+    assert 100.0 < bench.qk8_tensor_peak(peaks) < 200.0
+    # a compute-bound case picks that peak; a byte-bound one is unchanged
+    t_q8, bound = bench.roofline_time_s(10 ** 15, 10 ** 6, peaks, qk8=True)
+    assert bound == "tensor" and abs(t_q8 - 10 ** 15 / (bench.qk8_tensor_peak(peaks) * 1e12)) < 1e-12
+    assert bench.roofline_time_s(10 ** 6, 10 ** 12, peaks, qk8=True) == bench.roofline_time_s(10 ** 6, 10 ** 12, peaks)
